@@ -1,0 +1,470 @@
+#!/usr/bin/env python3
+"""Benchmark: NVFP4 paged decode on one or more GB300s (one process per GPU).
+
+One step = the step's new K/V tokens quantised into their pages
+(nvfp4kv_quantize_append) + paged NVFP4 attention (nvfp4kv_decode_attend)
++ the split-KV merge (nvfp4kv_decode_merge) over the long-context decode
+workload (B=4, Hq=32, Hkv=8, D=128, kv_len=32771, page_size 16).  The plan is
+built once, outside the timed region (as serving builds it once per batch
+step and reuses it for every layer); the end-to-end leg re-plans every step.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU
+oracle on the same workload instead (bounded samples per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import nvfp4_paged_kv_nvfp4kv_gb300 as N  # noqa: E402
+from nvfp4_paged_kv_nvfp4kv_gb300 import workloads as W  # noqa: E402
+
+METRIC = "NVFP4 paged decode: µs/call, KV tokens/s, achieved HBM GB/s vs GB300 peak"
+UNIT = "KV tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attend_tc_long_context_decode.json")
+KERNEL_SOURCES = [os.path.join(ROOT, "nvfp4_paged_kv_nvfp4kv_gb300", "csrc", f)
+                  for f in ("attend_tc.cu", "device_common.cuh", "internal.h")]
+
+
+def workload_desc(cfg: W.Workload) -> str:
+    lens = ("kv_len=%d" % cfg.kv_len_lo if cfg.kv_len_lo == cfg.kv_len_hi
+            else "kv_len~U[%d,%d]" % (cfg.kv_len_lo, cfg.kv_len_hi))
+    return ("%s: B=%d qo_len=%d Hq=%d Hkv=%d Dqk=%d Dvo=%d %s page_size=16%s, NVFP4 K/V "
+            "(e2m1 + E4M3 per 16)" % (cfg.name, cfg.batch, cfg.qo_len, cfg.num_qo_heads,
+                                      cfg.num_kv_heads, cfg.head_dim_qk, cfg.head_dim_vo,
+                                      lens, ", causal" if cfg.causal else ""))
+
+
+def algorithmic_bytes(batch: W.Batch) -> int:
+    """KV bytes at 0.5 B/element + scale bytes + Q + O + lse + page table."""
+    c = batch.cfg
+    kv = sum(batch.kv_lens) * c.num_kv_heads * (
+        c.head_dim_qk // 2 + c.head_dim_qk // 16 + c.head_dim_vo // 2 + c.head_dim_vo // 16)
+    rows = int(batch.qo_indptr[-1])
+    qo = rows * c.num_qo_heads * (2 * c.head_dim_qk + 2 * c.head_dim_vo + 4)
+    pt = 4 * (int(batch.kv_indices.numel()) + 2 * c.batch + 1 + c.batch + 1)
+    return kv + qo + pt
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_per_launch(n_units_kv_bytes: int):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("kernel_hash") != kernel_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while a region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self._t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def init_dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, world, rank, local):
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = W.WORKLOADS[args.workload]
+    batch = W.make_batch(cfg)
+    lay = batch.cache_layout(args.layout)
+    cache = N.PagedCache.allocate(lay, batch.k_global_scale, batch.v_global_scale,
+                                  device=dev)
+    i32 = lambda t: torch.as_tensor(t).to(torch.int32).to(dev)
+    kv_indices, kv_indptr, last = i32(batch.kv_indices), i32(batch.kv_indptr), \
+        i32(batch.last_page_len)
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    ts = batch.prefix
+    for s in range(0, ts.k.shape[0], 1 << 16):
+        N.nvfp4kv_quantize_append(cache, ts.k[s:s + (1 << 16)].to(dev),
+                                  ts.v[s:s + (1 << 16)].to(dev),
+                                  i32(ts.batch_idx[s:s + (1 << 16)]),
+                                  i32(ts.positions[s:s + (1 << 16)]), kv_indices, kv_indptr,
+                                  last, device_flags=flags)
+    new_k, new_v = batch.new.k.to(dev), batch.new.v.to(dev)
+    new_b, new_p = i32(batch.new.batch_idx), i32(batch.new.positions)
+    q = batch.q.to(dev)
+    c = cfg
+    plan = N.nvfp4kv_decode_plan(batch.qo_indptr, batch.kv_indptr, batch.last_page_len,
+                                 c.num_qo_heads, c.num_kv_heads, c.head_dim_qk, c.head_dim_vo,
+                                 causal=c.causal, kernel=args.kernel, device=local)
+    rows = int(batch.qo_indptr[-1])
+    out = torch.empty((rows, c.num_qo_heads, c.head_dim_vo), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((rows, c.num_qo_heads), dtype=torch.float32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        N.nvfp4kv_quantize_append(cache, new_k, new_v, new_b, new_p, kv_indices, kv_indptr,
+                                  last, device_flags=flags)
+        if ev:
+            ev[1].record(stream)
+        N.nvfp4kv_decode_attend(plan, q, cache, kv_indices, batch.sm_scale, out=out, lse=lse)
+        if ev:
+            ev[2].record(stream)
+        N.nvfp4kv_decode_merge(plan, out, lse)
+        if ev:
+            ev[3].record(stream)
+
+    def pre_step():
+        flush.fill_(1)              # evict the cache (> L2) between steps
+        torch.cuda._sleep(200000)   # bounded spin: keep the GPU busy while the
+        #                             host enqueues the step back to back
+
+    for _ in range(args.warmup):
+        pre_step()
+        step()
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 0
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for k in range(args.steps):
+            pre_step()
+            step(evs[k])
+        torch.cuda.synchronize()
+    barrier(world)
+    t_step = [e[0].elapsed_time(e[3]) for e in evs]
+    t_append = [e[0].elapsed_time(e[1]) for e in evs]
+    t_attend = [e[1].elapsed_time(e[2]) for e in evs]
+    t_merge = [e[2].elapsed_time(e[3]) for e in evs]
+    ms_step = statistics.mean(t_step)
+    ms_step_max = max_over_ranks(ms_step, world)
+    kv_tokens = sum(batch.kv_lens)
+    value = kv_tokens * world / (ms_step_max * 1e-3)
+
+    # ---- end to end through the public API with host buffers -------------
+    pin = lambda t: t.contiguous().pin_memory()
+    h_q, h_k, h_v = pin(batch.q), pin(batch.new.k), pin(batch.new.v)
+    h_b, h_p = pin(batch.new.batch_idx), pin(batch.new.positions)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(new_k), torch.empty_like(new_v)
+    d_b, d_p = torch.empty_like(new_b), torch.empty_like(new_p)
+    ws = plan.workspace
+    e2e_steps = max(3, min(args.steps, 200))
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_b, h_p))
+    h2d += int(plan.info.plan_host_bytes) + 4
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+    times = []
+    for k in range(e2e_steps + 3):
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_b, h_b), (d_p, h_p)):
+            d.copy_(h, non_blocking=True)
+        p2 = N.nvfp4kv_decode_plan(batch.qo_indptr, batch.kv_indptr, batch.last_page_len,
+                                   c.num_qo_heads, c.num_kv_heads, c.head_dim_qk,
+                                   c.head_dim_vo, causal=c.causal, kernel=args.kernel,
+                                   device=local, reuse=plan)
+        N.nvfp4kv_quantize_append(cache, d_k, d_v, d_b, d_p, kv_indices, kv_indptr, last,
+                                  device_flags=flags)
+        N.nvfp4kv_decode_run(p2, d_q, cache, kv_indices, batch.sm_scale, out=out, lse=lse)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        stream.synchronize()
+        if k >= 3:
+            times.append(time.perf_counter() - t0)
+    e2e_s = max_over_ranks(statistics.mean(times), world)
+    e2e_value = kv_tokens * world / e2e_s
+
+    # ---- roofline of the attention kernel -------------------------------
+    peak, peak_kind = measured_peak()
+    alg = algorithmic_bytes(batch)
+    ms_attend = statistics.mean(t_attend)
+    achieved = alg / (ms_attend * 1e-3) / 1e9
+    traffic = traffic_per_launch(alg)
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": workload_desc(cfg), "layout": args.layout,
+            "step": "quantize_append(new tokens) + attend + merge; plan built once",
+            "l2": "flushed between steps (512 MB write)",
+            "kernel": "tensor-core mma.sync f16/f32acc" if plan.info.kernel == 1 else
+                      "CUDA-core f32",
+            "split_units": int(plan.info.num_units), "split": int(plan.info.split),
+            "chunk_pages": int(plan.info.chunk_pages),
+            "us_per_call": ms_step_max * 1e3,
+            "us_attend": ms_attend * 1e3, "us_merge": statistics.mean(t_merge) * 1e3,
+            "us_append": statistics.mean(t_append) * 1e3,
+            "algorithmic_bytes_per_call": alg,
+            "hbm_gbs_step": alg / (ms_step_max * 1e-3) / 1e9,
+            "parallelism": "replicas (one independent batch per GPU)",
+        },
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": peak_kind},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": args.steps * (2 + (1 if plan.info.split else 0)),
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(batch, args.layout)
+    return result
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def _oracle():
+    sys.path.insert(0, os.path.join(ROOT, "oracle"))
+    import oracle as O
+    return O
+
+
+def _oracle_prefix_cache(batch, requests, layout):
+    O = _oracle()
+    c = O.Cache(batch.cache_layout(layout), batch.k_global_scale, batch.v_global_scale)
+    pt = O.PageTable.of(batch)
+    req = torch.tensor(sorted(requests))
+    for ts in (batch.prefix,):
+        m = torch.isin(ts.batch_idx, req.to(ts.batch_idx.dtype))
+        sub = W.TokenSet(ts.batch_idx[m], ts.positions[m], ts.k[m], ts.v[m])
+        assert O.quantize_append(c, pt, sub) == 0
+    return c, pt
+
+
+def _oracle_units(O, cache, pt, batch, units, threads, chunk=None):
+    """Oracle step on (request, kv head) units: append the requests' new
+    tokens, then exact attention, the units spread over a thread pool
+    (ctypes releases the GIL)."""
+    import concurrent.futures as cf
+    c = batch.cfg
+    reqs = sorted({b for b, _ in units})
+    m = torch.isin(batch.new.batch_idx, torch.tensor(reqs, dtype=batch.new.batch_idx.dtype))
+    sub = W.TokenSet(batch.new.batch_idx[m], batch.new.positions[m], batch.new.k[m],
+                     batch.new.v[m])
+    assert O.quantize_append(cache, pt, sub) == 0
+    rows = int(batch.qo_indptr[-1])
+    import numpy as np
+    out = np.full((rows, c.num_qo_heads, c.head_dim_vo), np.nan)
+    lse = np.full((rows, c.num_qo_heads), np.nan)
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(lambda u: O.attention(cache, pt, batch.qo_indptr, batch.q,
+                                          c.num_qo_heads, c.causal, batch.sm_scale,
+                                          units=[u], out=out, lse=lse), units))
+    return out, lse
+
+
+def cpu_baseline(batch, layout):
+    """The oracle as it stands on the host cores: up to 4 requests of the
+    workload, one (request, kv head) unit per thread."""
+    O = _oracle()
+    c = batch.cfg
+    requests = list(range(min(4, c.batch)))
+    cache, pt = _oracle_prefix_cache(batch, requests, layout)
+    units = [(b, h) for b in requests for h in range(c.num_kv_heads)]
+    threads = min(len(units), os.cpu_count() or 1)
+    t0 = time.perf_counter()
+    _oracle_units(O, cache, pt, batch, units, threads)
+    dt = time.perf_counter() - t0
+    toks = sum(batch.kv_lens[b] for b in requests)
+    return {"value": toks / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "requests %s of the workload (%d KV tokens x %d kv heads), append of "
+                      "their new tokens + float64 exact attention, %.1f s" % (
+                          requests, toks, c.num_kv_heads, dt)}
+
+
+def run_reference(args, world, rank):
+    """The oracle timed on the host cores: each step appends one request's new
+    token and runs exact attention for a bounded slice of its kv heads."""
+    if rank != 0:
+        return None
+    O = _oracle()
+    cfg = W.WORKLOADS[args.workload]
+    batch = W.make_batch(cfg)
+    req = 0
+    cache, pt = _oracle_prefix_cache(batch, [req], args.layout)
+    # Per-step sample: as many kv heads of the request as fit the time budget
+    # of the whole --warmup + --steps run (NVFP4KV_REF_BUDGET_S, default 150 s);
+    # if even one head per step is slower, the run stops at the budget and
+    # reports the steps it timed.
+    budget = float(os.environ.get("NVFP4KV_REF_BUDGET_S", "150"))
+    t0 = time.perf_counter()
+    _oracle_units(O, cache, pt, batch, [(req, 0)], 1)
+    unit_s = time.perf_counter() - t0
+    per_step = budget / max(1, args.steps + args.warmup)
+    heads = max(1, min(cfg.num_kv_heads, int(per_step / max(unit_s, 1e-9))))
+    threads = min(heads, os.cpu_count() or 1)
+    units = [(req, h) for h in range(heads)]
+    times = []
+    start = time.perf_counter()
+    for k in range(args.warmup + args.steps):
+        t = time.perf_counter()
+        _oracle_units(O, cache, pt, batch, units, threads)
+        if k >= args.warmup:
+            times.append(time.perf_counter() - t)
+        if len(times) >= 3 and time.perf_counter() - start > budget:
+            break
+    dt = statistics.mean(times)
+    toks = batch.kv_lens[req] * heads / cfg.num_kv_heads
+    value = toks / dt
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": len(times), "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "layout": args.layout,
+                   "sample": "request %d, %d of %d kv heads per step" % (
+                       req, heads, cfg.num_kv_heads)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": "request %d (%d KV tokens), %d kv heads per step" % (
+                             req, batch.kv_lens[req], heads)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="long_context_decode", choices=list(W.WORKLOADS))
+    ap.add_argument("--layout", default="HND", choices=["HND", "NHD"])
+    ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 tensor-core, 2 CUDA-core")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = init_dist()
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+    else:
+        res = run_gpu(args, world, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,257 @@
+/*
+ * nvfp4kv.h -- C ABI of the NVFP4 paged-KV attention library (GB300, sm_103a).
+ *
+ * Batched attention decode and short-query extend over a paged KV cache whose
+ * K and V are stored as NVFP4: e2m1 values packed two per byte (low nibble =
+ * even element), one FP8-E4M3 scale per 16 consecutive head-dim elements of a
+ * token, and one FP32 global scale per tensor (page "Support NVFP4 KV cache
+ * decode on SM120", Gemini changelog of csrc/xqa/mha.h: GMemCacheHeadSf and
+ * the k_sf_cache / v_sf_cache / kv_cache_sf arguments of xqa and
+ * xqa_batch_decode_with_kv_cache).
+ *
+ * Conventions shared by every entry point
+ *  - Every function returns an nvfp4kv_status (0 = success).  On failure
+ *    nvfp4kv_last_error_detail() returns a message for the calling thread.
+ *    Nothing aborts, throws across the ABI, allocates device memory or
+ *    synchronises a stream (nvfp4kv_workspace_flags excepted, which reads one
+ *    word back).  Argument errors are detected on the host before anything is
+ *    enqueued: a call that fails validation launches nothing.
+ *  - The caller owns every buffer.  Device buffers (marked [dev]) must stay
+ *    allocated until the work enqueued on `stream` has completed; host
+ *    buffers (marked [host]) are read during the call, except `plan_host`,
+ *    which is also the source of an asynchronous copy (see the plan).
+ *  - Cache tensors use BYTE strides; the innermost row (the Dk/2 or Dv/2
+ *    packed bytes, the Dk/16 or Dv/16 scale bytes of one (page, slot, head))
+ *    is contiguous.  K, V, K-scale and V-scale each have their own stride
+ *    triple, so K and V pools with different stride families are supported,
+ *    not silently mis-addressed (page "Re-enable split-KV for NVFP4 KV cache
+ *    in prefill path", commits on independent K/V strides and on the
+ *    support-or-reject contract).  NHD ([page][slot][head][row]) and HND
+ *    ([page][head][slot][row]) are both expressible.
+ *  - Q strides are in elements; out [rows, Hq, Dv] bf16 and lse [rows, Hq]
+ *    float32 are contiguous; the output is sized by head_dim_vo (same page,
+ *    commit on the asymmetric-head dispatch and out_head_dim sizing).
+ *  - lse is the natural log of the sum of exp of the scaled scores and is
+ *    written for every (query row, head) (page "fix(attention): correct
+ *    SM120 NVFP4 qk_correction layout, row-sum reduction, and lse", second
+ *    commit).
+ *  - Page table (FlashInfer convention): request b owns the pages
+ *    kv_indices[kv_indptr[b] .. kv_indptr[b+1]) and holds
+ *    L_b = (npages_b - 1) * page_size + last_page_len[b] tokens (0 when it
+ *    owns no page); qo_indptr gives its n_b = qo_indptr[b+1]-qo_indptr[b]
+ *    query rows, which sit at positions L_b - n_b .. L_b - 1 (bottom-right
+ *    causal alignment: a new token sees the whole prefix, the earlier new
+ *    tokens and itself).
+ */
+#ifndef NVFP4KV_H
+#define NVFP4KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status ------------------------------------------------------------ */
+typedef enum nvfp4kv_status {
+  NVFP4KV_OK = 0,
+  NVFP4KV_ERR_INVALID_ARGUMENT = 1,  /* null pointer, bad size/stride/index */
+  NVFP4KV_ERR_UNSUPPORTED = 2,       /* valid but not implemented here      */
+  NVFP4KV_ERR_WORKSPACE_TOO_SMALL = 3,
+  NVFP4KV_ERR_CUDA = 4,              /* a CUDA runtime call failed          */
+  NVFP4KV_ERR_DEVICE_CHECK = 5,      /* device flags report a bad index     */
+  NVFP4KV_ERR_PLAN_MISMATCH = 6      /* run arguments differ from the plan  */
+} nvfp4kv_status;
+
+/* Bits of the device flag word (see nvfp4kv_workspace_flags). */
+#define NVFP4KV_FLAG_BAD_PAGE_INDEX 0x1u   /* a kv_indices entry out of pool  */
+#define NVFP4KV_FLAG_BAD_APPEND_TARGET 0x2u /* append token outside its request */
+
+const char* nvfp4kv_status_string(int status);
+const char* nvfp4kv_last_error_detail(void);
+
+/* ---- the paged cache ----------------------------------------------------- */
+typedef struct nvfp4kv_paged_cache {
+  uint8_t* k_data; /* [dev] packed e2m1, Dk/2 bytes per (page, slot, head)   */
+  uint8_t* v_data; /* [dev] packed e2m1, Dv/2 bytes per (page, slot, head)   */
+  uint8_t* k_sf;   /* [dev] E4M3 bytes, Dk/16 per (page, slot, head)         */
+  uint8_t* v_sf;   /* [dev] E4M3 bytes, Dv/16 per (page, slot, head)         */
+  int64_t k_stride_page, k_stride_slot, k_stride_head;          /* bytes */
+  int64_t v_stride_page, v_stride_slot, v_stride_head;          /* bytes */
+  int64_t k_sf_stride_page, k_sf_stride_slot, k_sf_stride_head; /* bytes */
+  int64_t v_sf_stride_page, v_sf_stride_slot, v_sf_stride_head; /* bytes */
+  int32_t num_pages;   /* pages in the pool                                  */
+  int32_t page_size;   /* tokens per page; must be 16                        */
+  int32_t num_kv_heads;
+  int32_t head_dim_qk; /* (Dk, Dv) in {(64,64), (128,128), (256,256),        */
+  int32_t head_dim_vo; /*  (256,128), (512,256)}; others: UNSUPPORTED         */
+  float k_global_scale; /* dequantised K = e2m1 * E4M3 scale * k_global_scale */
+  float v_global_scale; /* dequantised V uses its own global scale           */
+} nvfp4kv_paged_cache;
+/* Alignment: data pointers and data strides are multiples of 16 bytes; scale
+ * pointers and scale strides are multiples of min(16, D/16) bytes. */
+
+/* ---- quantise-append ----------------------------------------------------- */
+/* Quantise nnz new tokens from bf16 and store them into their pages
+ * (the in-tree NVFP4 KV quantisation kernel the prefill tests of page
+ * "Re-enable split-KV for NVFP4 KV cache in prefill path" feed the cache
+ * with; recipe per 16-element block of one token and head: scale byte
+ * s = E4M3_RNE_satfinite(amax / (6 g)), codes e2m1_RNE_satfinite(x / (s g))
+ * with ties to the even code, zero codes keeping the sign of x, low nibble =
+ * even element; every rounding decision is the exact-real one).
+ *   k_bf16 [dev]  element (t, h, d) at k_bf16[t*k_stride_tok + h*k_stride_head
+ *                 + d]; strides in elements, multiples of 8; 16-byte aligned.
+ *   v_bf16 [dev]  same with the V strides, d < head_dim_vo.
+ *   batch_idx, positions [dev, nnz]  request and absolute position of token t.
+ *   kv_indices, kv_indptr, last_page_len [dev]  page table AFTER the append
+ *                 (every position must lie below L_b).
+ *   device_flags [dev, optional]  a token whose request, position or page id
+ *                 is out of range is skipped and sets
+ *                 NVFP4KV_FLAG_BAD_APPEND_TARGET here.
+ * Inputs must be finite.  nnz == 0 is a no-op. */
+int nvfp4kv_quantize_append(const nvfp4kv_paged_cache* cache,
+                            const void* k_bf16, int64_t k_stride_tok,
+                            int64_t k_stride_head, const void* v_bf16,
+                            int64_t v_stride_tok, int64_t v_stride_head,
+                            int32_t nnz, const int32_t* batch_idx,
+                            const int32_t* positions, const int32_t* kv_indices,
+                            const int32_t* kv_indptr,
+                            const int32_t* last_page_len, int32_t batch,
+                            uint32_t* device_flags, cudaStream_t stream);
+
+/* ---- plan ---------------------------------------------------------------- */
+/* Split-KV (flash-decoding) work plan.  Chunk boundaries are whole pages,
+ * i.e. multiples of 16 tokens (page "Re-enable split-KV for NVFP4 KV cache in
+ * prefill path": the commit gating split-KV off for NVFP4 and its follow-up
+ * asking for 16-token-aligned chunks; a later commit there notes that scale
+ * blocks run along head_dim, so a token-axis split never cuts one).  The
+ * plan sizes the chunk so the attention grid fills the GPU in one wave,
+ * reading the SM count and the per-block shared-memory opt-in of the device
+ * (same page, commit on the shared-memory probe). */
+typedef struct nvfp4kv_plan_options {
+  int32_t causal;             /* nonzero: causal (bottom-right) within a row  */
+  int32_t disable_split;      /* nonzero: one work unit per (request, head)  */
+  int32_t max_splits;         /* >0: at most this many chunks per request    */
+  int32_t force_chunk_tokens; /* >0: chunk size in tokens, multiple of 16    */
+  int32_t kernel;             /* 0 auto, 1 tensor-core (mma), 2 CUDA-core    */
+  int32_t num_sms;            /* >0: override the device's SM count          */
+  int32_t ctas_per_sm;        /* >0: override the occupancy query            */
+  int32_t reserved[5];
+} nvfp4kv_plan_options;
+
+typedef struct nvfp4kv_plan_info {
+  uint32_t magic;
+  int32_t batch, num_qo_heads, num_kv_heads, head_dim_qk, head_dim_vo;
+  int32_t page_size, causal;
+  int32_t kernel;          /* 1 tensor-core, 2 CUDA-core                     */
+  int32_t num_units;       /* attention work units (grid x)                  */
+  int32_t row_blocks;      /* query-row blocks per unit (grid y)             */
+  int32_t rows_per_block;  /* query rows (G x qo positions) per CTA          */
+  int32_t warps;           /* warps per CTA                                  */
+  int32_t split;           /* nonzero: partial states + merge                */
+  int32_t chunk_pages;     /* pages per unit (the last one may be shorter)   */
+  int32_t max_units_per_request;
+  int32_t total_qo_rows;   /* sum of n_b                                     */
+  int32_t num_sms, ctas_per_sm, smem_bytes, device;
+  int64_t num_partials;    /* partial (o, lse) states when split             */
+  int64_t total_kv_pages;  /* pages referenced by the batch                  */
+  uint64_t workspace_bytes;  /* device workspace needed                      */
+  uint64_t plan_host_bytes;  /* host bytes the plan writes into plan_host    */
+  uint64_t off_flags, off_units, off_merge_indptr, off_partial_lse,
+      off_partial_o;       /* byte offsets inside the workspace              */
+} nvfp4kv_plan_info;
+
+/* Build the plan from HOST copies of the batch description.
+ *   qo_indptr_h, kv_indptr_h [host, batch+1], last_page_len_h [host, batch].
+ *   opts [host, may be NULL = defaults].
+ *   device  CUDA device to plan for (<0: current device; when both num_sms
+ *           and ctas_per_sm are given no device is queried at all).
+ *   plan_host [host] receives the work list; it must hold
+ *           info->plan_host_bytes.  When workspace is non-NULL the plan
+ *           enqueues one cudaMemcpyAsync(workspace <- plan_host) and a
+ *           cudaMemsetAsync of the flag word on `stream`: keep plan_host
+ *           unchanged until that copy completes (use pinned memory to keep
+ *           it asynchronous).
+ *   workspace [dev, may be NULL]: NULL asks for sizes only (info filled,
+ *           nothing enqueued); otherwise it must hold info->workspace_bytes
+ *           and be 256-byte aligned.
+ * Returns WORKSPACE_TOO_SMALL (with info sizes filled) when plan_host or the
+ * workspace is too small. */
+int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
+                        const int32_t* last_page_len_h, int32_t batch,
+                        int32_t num_qo_heads, int32_t num_kv_heads,
+                        int32_t head_dim_qk, int32_t head_dim_vo,
+                        int32_t page_size, const nvfp4kv_plan_options* opts,
+                        int32_t device, void* plan_host,
+                        uint64_t plan_host_bytes, void* workspace,
+                        uint64_t workspace_bytes, cudaStream_t stream,
+                        nvfp4kv_plan_info* info);
+
+/* ---- run ------------------------------------------------------------------ */
+/* Attention for the planned batch: GQA-grouped QK^T, online softmax and PV
+ * over the dequantised pages, then (when the plan split the work) the
+ * log-sum-exp merge.  Calls only kernels: it can be captured in a CUDA graph.
+ *   q_bf16 [dev]  element (row, head, d) at q[row*q_stride_tok +
+ *                 head*q_stride_head + d]; strides in elements, multiples
+ *                 of 8; 16-byte aligned.
+ *   cache         the paged cache (dims must match the plan).
+ *   kv_indices [dev]  the planned page table's page ids.
+ *   sm_scale      scale of the scores; <= 0 selects 1/sqrt(head_dim_qk).
+ *   workspace [dev]   the workspace the plan was uploaded into.
+ *   out_bf16 [dev]    [rows, Hq, Dv]; lse [dev, may be NULL] [rows, Hq].
+ * A page id outside the pool is read as page 0 and sets
+ * NVFP4KV_FLAG_BAD_PAGE_INDEX in the workspace flag word. */
+int nvfp4kv_decode_run(const nvfp4kv_plan_info* info, const void* q_bf16,
+                       int64_t q_stride_tok, int64_t q_stride_head,
+                       const nvfp4kv_paged_cache* cache,
+                       const int32_t* kv_indices, float sm_scale,
+                       void* workspace, uint64_t workspace_bytes,
+                       void* out_bf16, float* lse, cudaStream_t stream);
+
+/* The two halves of nvfp4kv_decode_run, for callers that time or overlap
+ * them: the attention kernel (writes out/lse directly when the plan has no
+ * split, partial states into the workspace otherwise) and the merge of the
+ * plan's partial states (a no-op without split). */
+int nvfp4kv_decode_attend(const nvfp4kv_plan_info* info, const void* q_bf16,
+                          int64_t q_stride_tok, int64_t q_stride_head,
+                          const nvfp4kv_paged_cache* cache,
+                          const int32_t* kv_indices, float sm_scale,
+                          void* workspace, uint64_t workspace_bytes,
+                          void* out_bf16, float* lse, cudaStream_t stream);
+int nvfp4kv_decode_merge(const nvfp4kv_plan_info* info, void* workspace,
+                         uint64_t workspace_bytes, void* out_bf16, float* lse,
+                         cudaStream_t stream);
+
+/* ---- merge ---------------------------------------------------------------- */
+/* Fold partial attention states (the flash-decoding split of page
+ * "Re-enable split-KV for NVFP4 KV cache in prefill path"; the pages give no
+ * formula, this is the standard one): for entry e with partials
+ * i in [merge_indptr[e], merge_indptr[e+1]):
+ *   M = max_i lse_i;  lse = M + ln sum_i exp(lse_i - M);
+ *   o = sum_i exp(lse_i - lse) * o_i   (o_i already normalised);
+ * all lse_i = -inf, or no partial, gives o = 0 and lse = -inf.
+ *   o_partial [dev] float32 [num_partials, head_dim_vo];
+ *   lse_partial [dev] float32 [num_partials], natural log;
+ *   merge_indptr [dev] int32 [num_entries + 1];
+ *   out_bf16 [dev] [num_entries, head_dim_vo]; lse [dev, may be NULL]
+ *   [num_entries].  head_dim_vo is a multiple of 32, at most 512. */
+int nvfp4kv_merge_states(const float* o_partial, const float* lse_partial,
+                         const int32_t* merge_indptr, int32_t num_entries,
+                         int32_t head_dim_vo, void* out_bf16, float* lse,
+                         cudaStream_t stream);
+
+/* ---- flags ---------------------------------------------------------------- */
+/* Read (and optionally clear) the device flag word of a planned workspace.
+ * Synchronises `stream`.  Returns NVFP4KV_ERR_DEVICE_CHECK when a flag is set
+ * (the word is still written to *flags). */
+int nvfp4kv_workspace_flags(const nvfp4kv_plan_info* info,
+                            const void* workspace, uint32_t* flags,
+                            int32_t clear, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4KV_H */

@@ -1,0 +1,515 @@
+// attend_tc.cu -- paged NVFP4 decode / extend attention on the tensor cores
+// (mma.sync m16n8k16, f16 operands, f32 accumulators), sm_103a.
+//
+// What it computes (page "Support NVFP4 KV cache decode on SM120": packed
+// e2m1 K/V with per-16 E4M3 scale caches, unpacked and scaled before the
+// QK and PV products; page "fix(attention): correct SM120 NVFP4
+// qk_correction layout, row-sum reduction, and lse": row reductions over
+// exactly the lanes that own a row, lse written as natural-log sum-exp):
+//   s_j = sm_scale * sum_d q_d * k_hat_{j,d},  online softmax over the
+//   visible keys, o = sum_j p_j v_hat_j / sum_j p_j, lse = ln sum_j exp s_j.
+//
+// Design (one work unit = (request, kv head, chunk of pages) x a block of up
+// to 16 query rows; the G heads of the group times the query positions):
+//  * Each warp owns every WARPS-th page of the chunk and streams it through
+//    its own STAGES-deep cp.async ring in shared memory (16-byte copies of the
+//    packed K/V rows and the scale rows; any byte strides, NHD or HND).
+//  * QK^T: S = Q . K_hat^T with M = query rows, N = 8 tokens, K = 16 dims.
+//    The B operand wants two adjacent dims of one token per register, which
+//    is exactly one packed byte: cvt.rn.f16x2.e2m1x2 then one f16x2 multiply
+//    by the block scale (code * E4M3 scale is exact in f16).  The contraction
+//    dims are permuted so each lane reads 16 contiguous bytes of a token row;
+//    Q is permuted identically when its fragments are built.
+//  * Global scales stay out of the f16 operands: g_K is folded into the f32
+//    score scale, g_V into the epilogue.  Q is multiplied by a power of two
+//    per row (exact) so its bf16 values land in f16's normal range.
+//  * PV: O^T = V_hat^T . P^T with M = 16 value dims, N = 8 query rows,
+//    K = 16 tokens; the S accumulator layout is already the P^T B-fragment
+//    layout, so P never leaves registers.  The A operand needs pairs of
+//    tokens per dim: two converted bytes are interleaved with one byte_perm
+//    each, and multiplied by the pair of per-token scales.
+//  * Online softmax in the log2 domain; the max and sum reductions run over
+//    the 4 lanes (xor 1, 2) that hold one row.  Warps combine through shared
+//    memory; the unit writes bf16 out + lse, or an f32 partial state + lse
+//    for the merge when the plan split the request.
+#include <cfloat>
+#include <cstdint>
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace nvfp4kv {
+namespace {
+
+using namespace dev;
+
+template <int DK, int DV, int NT, int WARPS, int STAGES>
+struct TcTraits {
+  static constexpr int RB = 8 * NT;                  // query rows per CTA
+  static constexpr int CB = (DK / 8 < 16) ? DK / 8 : 16;  // K bytes per lane chunk
+  static constexpr int NCH = (DK / 8) / CB;          // K chunks per lane
+  static constexpr int KSTEPS = DK / 16;
+  static constexpr int KS_PER_CH = CB / 2;
+  static constexpr int KROW = DK / 2;                // smem row of packed K
+  static constexpr bool KSWZ = DK >= 256;            // xor-swizzle odd rows
+  static constexpr int KSFROW = DK / 16;
+  static constexpr int VC = DV / 16;                 // V bytes per lane per token
+  // padded V row: the PV reads (lane group g, tokens 2t..) hit distinct banks
+  static constexpr int VROW = DV / 2 + 16;
+  static constexpr int VSFROW = DV / 16;
+  static constexpr int MT = DV / 16;                 // PV m-tiles
+  static constexpr int K_BYTES = 16 * KROW;
+  static constexpr int KSF_BYTES = 16 * KSFROW;
+  static constexpr int V_BYTES = 16 * VROW;
+  static constexpr int VSF_BYTES = 16 * VSFROW;
+  static constexpr int OFF_KSF = K_BYTES;
+  static constexpr int OFF_V = (OFF_KSF + KSF_BYTES + 15) / 16 * 16;
+  static constexpr int OFF_VSF = OFF_V + V_BYTES;
+  static constexpr int STAGE_BYTES = (OFF_VSF + VSF_BYTES + 15) / 16 * 16;
+  static constexpr int PIPE_BYTES = WARPS * STAGES * STAGE_BYTES;
+  static constexpr int COMB_BYTES = WARPS * RB * (DV + 2) * 4;
+  static constexpr int MAIN_BYTES = PIPE_BYTES > COMB_BYTES ? PIPE_BYTES : COMB_BYTES;
+  static constexpr int QROW = DK + 8;                // f16 elements, padded
+  static constexpr int Q_BYTES = RB * QROW * 2;
+  static constexpr int SMEM = MAIN_BYTES + Q_BYTES + RB * 16;
+  static constexpr bool Q_IN_REGS = KSTEPS * 2 * NT <= 32;
+  static_assert(DK % 64 == 0 && DV % 64 == 0, "head dims");
+  static_assert(VROW % 16 == 0, "V rows must stay 16-byte aligned");
+};
+
+// Copy one page (16 tokens of one kv head) into a warp's stage.
+template <class T>
+__device__ __forceinline__ void issue_page(uint8_t* st, const CacheView& c,
+                                           int32_t pid, int h, int lane) {
+  const uint8_t* kb = c.k_data + pid * c.k_sp + h * c.k_sh;
+  const uint8_t* vb = c.v_data + pid * c.v_sp + h * c.v_sh;
+  const uint8_t* ksb = c.k_sf + pid * c.ksf_sp + h * c.ksf_sh;
+  const uint8_t* vsb = c.v_sf + pid * c.vsf_sp + h * c.vsf_sh;
+  constexpr int KCH = T::KROW / 16;      // 16-byte chunks per K row
+  constexpr int VCHR = (T::VC * 8) / 16;  // 16-byte chunks per V row (DV/32)
+#pragma unroll
+  for (int ci = lane; ci < 16 * KCH; ci += 32) {
+    const int r = ci / KCH, ch = ci % KCH;
+    const int pos = T::KSWZ ? (ch ^ ((r & 1) << 2)) : ch;
+    cp_async_16(st + r * T::KROW + pos * 16, kb + r * c.k_ss + ch * 16);
+  }
+#pragma unroll
+  for (int ci = lane; ci < 16 * VCHR; ci += 32) {
+    const int r = ci / VCHR, ch = ci % VCHR;
+    cp_async_16(st + T::OFF_V + r * T::VROW + ch * 16, vb + r * c.v_ss + ch * 16);
+  }
+  // scale rows: KSFROW bytes per token, copied in units of min(16, KSFROW)
+  constexpr int KSU = T::KSFROW < 16 ? T::KSFROW : 16;
+  constexpr int KSN = T::KSFROW / KSU;
+#pragma unroll
+  for (int ci = lane; ci < 16 * KSN; ci += 32) {
+    const int r = ci / KSN, u = ci % KSN;
+    cp_async_small<KSU>(st + T::OFF_KSF + r * T::KSFROW + u * KSU,
+                        ksb + r * c.ksf_ss + u * KSU);
+  }
+  constexpr int VSU = T::VSFROW < 16 ? T::VSFROW : 16;
+  constexpr int VSN = T::VSFROW / VSU;
+#pragma unroll
+  for (int ci = lane; ci < 16 * VSN; ci += 32) {
+    const int r = ci / VSN, u = ci % VSN;
+    cp_async_small<VSU>(st + T::OFF_VSF + r * T::VSFROW + u * VSU,
+                        vsb + r * c.vsf_ss + u * VSU);
+  }
+}
+
+template <int DK, int DV, int NT, int WARPS, int STAGES>
+__global__ void __launch_bounds__(WARPS * 32)
+    attend_tc_kernel(const AttendParams p) {
+  using T = TcTraits<DK, DV, NT, WARPS, STAGES>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* pipe = smem;
+  uint16_t* sQ = reinterpret_cast<uint16_t*>(smem + T::MAIN_BYTES);
+  float* sRowF = reinterpret_cast<float*>(smem + T::MAIN_BYTES + T::Q_BYTES);
+  int* sRowLim = reinterpret_cast<int*>(sRowF + T::RB);
+
+  const WorkUnit u = p.units[blockIdx.x];
+  const int G = p.group;
+  const int R = G * u.qo_len;
+  const int row0 = blockIdx.y * T::RB;
+  if (row0 >= R) return;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int Hq = p.num_qo_heads;
+
+  // ---- Q: load, per-row power-of-two prescale into f16, row limits -------
+  for (int rr = warp; rr < T::RB; rr += WARPS) {
+    const int r = row0 + rr;
+    uint16_t* dst = sQ + rr * T::QROW;
+    if (r >= R) {
+      for (int d = lane; d < DK; d += 32) dst[d] = 0;
+      if (lane == 0) {
+        sRowF[rr] = 0.f;
+        sRowLim[rr] = -1;
+      }
+      continue;
+    }
+    const int i = r / G, gh = r % G;
+    const uint16_t* src = p.q + (int64_t)(u.qo_begin + i) * p.q_stride_tok +
+                          (int64_t)(u.h_kv * G + gh) * p.q_stride_head;
+    float amax = 0.f;
+    for (int d = lane; d < DK; d += 32)
+      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(src[d])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    // e such that amax * 2^e lies in [2^14, 2^15)
+    int e = 0;
+    if (amax > 0.f) e = 14 - (int)((__float_as_uint(amax) >> 23) & 0xFF) + 127;
+    e = max(-120, min(120, e));
+    const float up = __uint_as_float((uint32_t)(127 + e) << 23);
+    for (int d = lane; d < DK; d += 32)
+      dst[d] = __half_as_ushort(__float2half_rn(bf16_bits_to_f32(src[d]) * up));
+    if (lane == 0) {
+      sRowF[rr] = p.qk_scale_log2 * __uint_as_float((uint32_t)(127 - e) << 23);
+      sRowLim[rr] = p.causal ? (u.kv_len - u.qo_len + i) : (u.kv_len - 1);
+    }
+  }
+  __syncthreads();
+
+  // per-lane row data: rows g (half 0) and g + 8 (half 1)
+  float rowf[NT];
+  int rowlim[NT];
+  int min_lim = INT32_MAX;
+#pragma unroll
+  for (int hf = 0; hf < NT; ++hf) {
+    rowf[hf] = sRowF[8 * hf + g];
+    rowlim[hf] = sRowLim[8 * hf + g];
+  }
+  for (int rr = 0; rr < T::RB; ++rr)
+    if (sRowLim[rr] >= 0) min_lim = min(min_lim, sRowLim[rr]);
+
+  // Q fragments: k-step kk of chunk c = kk / KS_PER_CH, step m within it,
+  // covers the 4 consecutive dims starting at 2*(4c+t)*CB + 4m.
+  auto q_frag = [&](int kk, uint32_t (&a)[4]) {
+    const int c = kk / T::KS_PER_CH, m = kk % T::KS_PER_CH;
+    const int d0 = 2 * (4 * c + t) * T::CB + 4 * m;
+    const uint2 lo = *reinterpret_cast<const uint2*>(sQ + g * T::QROW + d0);
+    a[0] = lo.x;
+    a[2] = lo.y;
+    if constexpr (NT == 2) {
+      const uint2 hi = *reinterpret_cast<const uint2*>(sQ + (g + 8) * T::QROW + d0);
+      a[1] = hi.x;
+      a[3] = hi.y;
+    } else {
+      a[1] = 0u;
+      a[3] = 0u;
+    }
+  };
+  uint32_t qreg[T::Q_IN_REGS ? T::KSTEPS : 1][4];
+  if constexpr (T::Q_IN_REGS) {
+#pragma unroll
+    for (int kk = 0; kk < T::KSTEPS; ++kk) q_frag(kk, qreg[kk]);
+  }
+
+  // ---- per-warp state --------------------------------------------------
+  float m_run[NT], l_run[NT];
+  float oacc[T::MT][NT][4];
+#pragma unroll
+  for (int hf = 0; hf < NT; ++hf) {
+    m_run[hf] = -INFINITY;
+    l_run[hf] = 0.f;
+  }
+#pragma unroll
+  for (int mt = 0; mt < T::MT; ++mt)
+#pragma unroll
+    for (int nq = 0; nq < NT; ++nq)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) oacc[mt][nq][k] = 0.f;
+
+  uint8_t* wpipe = pipe + warp * STAGES * T::STAGE_BYTES;
+  const int npw = u.num_pages > warp ? (u.num_pages - warp + WARPS - 1) / WARPS : 0;
+  const int32_t* pidx = p.kv_indices + u.page_begin;
+
+  auto load_page = [&](int i) {
+    int32_t pid = pidx[warp + i * WARPS];
+    if (pid < 0 || pid >= p.cache.num_pages) {
+      if (lane == 0) atomicOr(p.flags, 0x1u);
+      pid = 0;
+    }
+    issue_page<T>(wpipe + (i % STAGES) * T::STAGE_BYTES, p.cache, pid, u.h_kv, lane);
+  };
+
+#pragma unroll
+  for (int s = 0; s < STAGES - 1; ++s) {
+    if (s < npw) load_page(s);
+    cp_async_commit();
+  }
+
+  for (int i = 0; i < npw; ++i) {
+    if (i + STAGES - 1 < npw) load_page(i + STAGES - 1);
+    cp_async_commit();
+    cp_async_wait<STAGES - 1>();
+    __syncwarp();
+    const uint8_t* st = wpipe + (i % STAGES) * T::STAGE_BYTES;
+    const int tok0 = u.tok_begin + (warp + i * WARPS) * 16;
+
+    // ---- S = Q K^T for tokens tok0 .. tok0+15 (two n-tiles) -------------
+    float sacc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sacc[nt][k] = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int row = 8 * nt + g;
+#pragma unroll
+      for (int c = 0; c < T::NCH; ++c) {
+        const int ch = 4 * c + t;
+        uint32_t w[T::CB / 4];
+        uint32_t sc0, sc1;
+        if constexpr (T::CB == 16) {
+          const int pos = T::KSWZ ? (ch ^ ((row & 1) << 2)) : ch;
+          const uint4 v = *reinterpret_cast<const uint4*>(st + row * T::KROW + pos * 16);
+          w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+          const uint32_t sfp = *reinterpret_cast<const uint16_t*>(
+              st + T::OFF_KSF + row * T::KSFROW + 2 * ch);
+          const uint32_t s2 = e4m3x2_to_f16x2(sfp);
+          sc0 = bcast_lo(s2);
+          sc1 = bcast_hi(s2);
+        } else {
+          const uint2 v = *reinterpret_cast<const uint2*>(st + row * T::KROW + ch * 8);
+          w[0] = v.x; w[1] = v.y;
+          const uint32_t sfb = st[T::OFF_KSF + row * T::KSFROW + ch];
+          sc0 = bcast_lo(e4m3x2_to_f16x2(sfb));
+          sc1 = sc0;
+        }
+#pragma unroll
+        for (int q = 0; q < T::CB / 4; ++q) {
+          uint32_t h[4];
+          e2m1x8_to_f16x8(w[q], h);
+          const uint32_t sc = (T::CB == 16 && q >= 2) ? sc1 : sc0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) h[j] = hmul2(h[j], sc);
+          const int kk = c * T::KS_PER_CH + 2 * q;
+          uint32_t a0[4], a1[4];
+          if constexpr (T::Q_IN_REGS) {
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              a0[x] = qreg[kk][x];
+              a1[x] = qreg[kk + 1][x];
+            }
+          } else {
+            q_frag(kk, a0);
+            q_frag(kk + 1, a1);
+          }
+          mma_16816(sacc[nt], a0, h[0], h[1]);
+          mma_16816(sacc[nt], a1, h[2], h[3]);
+        }
+      }
+    }
+
+    // ---- online softmax (log2 domain), rows g and g+8 -------------------
+    const bool need_mask = tok0 + 15 > min_lim;
+    uint32_t pfrag[NT][2];
+    float corr[NT];
+#pragma unroll
+    for (int hf = 0; hf < NT; ++hf) {
+      float x[4] = {sacc[0][2 * hf] * rowf[hf], sacc[0][2 * hf + 1] * rowf[hf],
+                    sacc[1][2 * hf] * rowf[hf], sacc[1][2 * hf + 1] * rowf[hf]};
+      if (need_mask) {
+        const int j0 = tok0 + 2 * t;
+        if (j0 > rowlim[hf]) x[0] = -INFINITY;
+        if (j0 + 1 > rowlim[hf]) x[1] = -INFINITY;
+        if (j0 + 8 > rowlim[hf]) x[2] = -INFINITY;
+        if (j0 + 9 > rowlim[hf]) x[3] = -INFINITY;
+      }
+      float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_run[hf], mx);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      corr[hf] = ex2(m_run[hf] - m_use);
+      m_run[hf] = m_new;
+      const float p0 = ex2(x[0] - m_use), p1 = ex2(x[1] - m_use);
+      const float p2 = ex2(x[2] - m_use), p3 = ex2(x[3] - m_use);
+      l_run[hf] = l_run[hf] * corr[hf] + ((p0 + p1) + (p2 + p3));
+      pfrag[hf][0] = f32x2_to_f16x2(p0, p1);
+      pfrag[hf][1] = f32x2_to_f16x2(p2, p3);
+    }
+    // rescale O^T columns (query rows 8nq+2t, 8nq+2t+1)
+#pragma unroll
+    for (int nq = 0; nq < NT; ++nq) {
+      const float cA = __shfl_sync(0xffffffffu, corr[nq], (2 * t) * 4);
+      const float cB = __shfl_sync(0xffffffffu, corr[nq], (2 * t + 1) * 4);
+#pragma unroll
+      for (int mt = 0; mt < T::MT; ++mt) {
+        oacc[mt][nq][0] *= cA;
+        oacc[mt][nq][1] *= cB;
+        oacc[mt][nq][2] *= cA;
+        oacc[mt][nq][3] *= cB;
+      }
+    }
+
+    // ---- O^T += V_hat^T P^T ---------------------------------------------
+    // tokens 2t, 2t+1, 2t+8, 2t+9; lane group g owns bytes [g*VC, g*VC+VC)
+    {
+      const uint8_t* vrow = st + T::OFF_V + g * T::VC;
+      const int tk[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+      constexpr int VW = T::VC / 4 > 0 ? T::VC / 4 : 1;  // 32-bit words per lane
+      uint32_t vw[4][VW];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint8_t* src = vrow + tk[k] * T::VROW;
+        if constexpr (T::VC == 16) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src);
+          vw[k][0] = v.x; vw[k][1] = v.y; vw[k][2] = v.z; vw[k][3] = v.w;
+        } else if constexpr (T::VC == 8) {
+          const uint2 v = *reinterpret_cast<const uint2*>(src);
+          vw[k][0] = v.x; vw[k][1] = v.y;
+        } else {
+          vw[k][0] = *reinterpret_cast<const uint32_t*>(src);
+        }
+      }
+      // per-token scale pairs for each scale block the lane's bytes touch
+      // Slots past kv_len on the request's last page hold whatever the pool
+      // held (possibly a NaN scale byte); their p is 0, but 0 * NaN would
+      // still poison the product, so their V scales are forced to 0.
+      const int valid = u.kv_len - tok0;  // tokens of this page that exist
+      constexpr int NBL = (T::VC * 2 + 15) / 16;
+      uint32_t sA[NBL], sB[NBL];
+#pragma unroll
+      for (int bl = 0; bl < NBL; ++bl) {
+        const int blk = (g * T::VC * 2) / 16 + bl;
+        const uint8_t* sfs = st + T::OFF_VSF + blk;
+        uint32_t s0 = sfs[tk[0] * T::VSFROW], s1 = sfs[tk[1] * T::VSFROW];
+        uint32_t s2 = sfs[tk[2] * T::VSFROW], s3 = sfs[tk[3] * T::VSFROW];
+        if (valid < 16) {
+          if (tk[0] >= valid) s0 = 0;
+          if (tk[1] >= valid) s1 = 0;
+          if (tk[2] >= valid) s2 = 0;
+          if (tk[3] >= valid) s3 = 0;
+        }
+        sA[bl] = e4m3x2_to_f16x2(s0 | (s1 << 8));
+        sB[bl] = e4m3x2_to_f16x2(s2 | (s3 << 8));
+      }
+#pragma unroll
+      for (int wq = 0; wq < VW; ++wq) {
+        uint32_t h[4][4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) e2m1x8_to_f16x8(vw[k][wq], h[k]);
+#pragma unroll
+        for (int j = 0; j < 4 && 4 * wq + j < T::VC; ++j) {
+          const int mt = 4 * wq + j;
+          const int bl = (mt * 2) / 16;
+          uint32_t a[4];
+          a[0] = hmul2(pack_lo(h[0][j], h[1][j]), sA[bl]);
+          a[1] = hmul2(pack_hi(h[0][j], h[1][j]), sA[bl]);
+          a[2] = hmul2(pack_lo(h[2][j], h[3][j]), sB[bl]);
+          a[3] = hmul2(pack_hi(h[2][j], h[3][j]), sB[bl]);
+#pragma unroll
+          for (int nq = 0; nq < NT; ++nq)
+            mma_16816(oacc[mt][nq], a, pfrag[nq][0], pfrag[nq][1]);
+        }
+      }
+    }
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+
+  // ---- combine the warps ------------------------------------------------
+#pragma unroll
+  for (int hf = 0; hf < NT; ++hf) {
+    l_run[hf] += __shfl_xor_sync(0xffffffffu, l_run[hf], 1);
+    l_run[hf] += __shfl_xor_sync(0xffffffffu, l_run[hf], 2);
+  }
+  __syncthreads();  // every warp is done with its pipeline buffers
+  float* sO = reinterpret_cast<float*>(pipe);           // [WARPS][RB][DV]
+  float* sM = sO + WARPS * T::RB * DV;                  // [WARPS][RB]
+  float* sL = sM + WARPS * T::RB;                       // [WARPS][RB]
+  if (t == 0) {
+#pragma unroll
+    for (int hf = 0; hf < NT; ++hf) {
+      sM[warp * T::RB + 8 * hf + g] = m_run[hf];
+      sL[warp * T::RB + 8 * hf + g] = l_run[hf];
+    }
+  }
+#pragma unroll
+  for (int mt = 0; mt < T::MT; ++mt) {
+    const int vb = g * T::VC + mt;  // byte of the V row -> dims 2vb, 2vb+1
+#pragma unroll
+    for (int nq = 0; nq < NT; ++nq) {
+      float* o0 = sO + (warp * T::RB + 8 * nq + 2 * t) * DV + 2 * vb;
+      float* o1 = o0 + DV;
+      *reinterpret_cast<float2*>(o0) = make_float2(oacc[mt][nq][0], oacc[mt][nq][2]);
+      *reinterpret_cast<float2*>(o1) = make_float2(oacc[mt][nq][1], oacc[mt][nq][3]);
+    }
+  }
+  __syncthreads();
+
+  const float kLn2 = 0.69314718055994530942f;
+  for (int idx = tid; idx < T::RB * (DV / 2); idx += WARPS * 32) {
+    const int rr = idx / (DV / 2), d = 2 * (idx % (DV / 2));
+    const int r = row0 + rr;
+    if (r >= R) continue;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) M = fmaxf(M, sM[w * T::RB + rr]);
+    float L = 0.f, o0 = 0.f, o1 = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < WARPS; ++w) {
+        const float mw = sM[w * T::RB + rr];
+        const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+        L += sL[w * T::RB + rr] * sc;
+        const float2 ow = *reinterpret_cast<const float2*>(sO + (w * T::RB + rr) * DV + d);
+        o0 += ow.x * sc;
+        o1 += ow.y * sc;
+      }
+      const float inv = p.v_scale / L;
+      o0 *= inv;
+      o1 *= inv;
+    }
+    const float lse_v = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
+    const int i = r / G, head = u.h_kv * G + r % G;
+    const int64_t qrow = u.qo_begin + i;
+    if (!p.split) {
+      const uint32_t packed = (uint32_t)f32_to_bf16_bits(o0) | ((uint32_t)f32_to_bf16_bits(o1) << 16);
+      *reinterpret_cast<uint32_t*>(p.out + (qrow * Hq + head) * DV + d) = packed;
+      if (d == 0 && p.lse) p.lse[qrow * Hq + head] = lse_v;
+    } else {
+      const int64_t pi = (int64_t)u.partial_base +
+                         ((int64_t)i * Hq + head) * u.num_splits + u.split;
+      *reinterpret_cast<float2*>(p.partial_o + pi * DV + d) = make_float2(o0, o1);
+      if (d == 0) p.partial_lse[pi] = lse_v;
+    }
+  }
+}
+
+template <int DK, int DV, int NT>
+bool make_tc(AttendConfig* cfg) {
+  constexpr int WARPS = 4, STAGES = DK >= 512 ? 3 : 4;
+  using T = TcTraits<DK, DV, NT, WARPS, STAGES>;
+  cfg->kind = kKernelTensorCore;
+  cfg->dk = DK;
+  cfg->dv = DV;
+  cfg->rows = T::RB;
+  cfg->warps = WARPS;
+  cfg->smem_bytes = T::SMEM;
+  cfg->func = reinterpret_cast<const void*>(attend_tc_kernel<DK, DV, NT, WARPS, STAGES>);
+  return true;
+}
+
+}  // namespace
+
+bool attend_config_tc(int dk, int dv, int rows, AttendConfig* cfg) {
+  const int nt = rows <= 8 ? 1 : 2;
+#define NVFP4KV_TC_CASE(DK_, DV_)                                      \
+  if (dk == DK_ && dv == DV_) return nt == 1 ? make_tc<DK_, DV_, 1>(cfg) \
+                                             : make_tc<DK_, DV_, 2>(cfg);
+  NVFP4KV_TC_CASE(64, 64)
+  NVFP4KV_TC_CASE(128, 128)
+  NVFP4KV_TC_CASE(256, 256)
+  NVFP4KV_TC_CASE(256, 128)
+  NVFP4KV_TC_CASE(512, 256)
+#undef NVFP4KV_TC_CASE
+  return false;
+}
+
+}  // namespace nvfp4kv

@@ -1,0 +1,125 @@
+// device_common.cuh -- small device helpers (inline PTX written from the PTX
+// ISA) used by the attention kernels.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace nvfp4kv {
+namespace dev {
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// cp.async: 16-byte global->shared copy bypassing L1 (.cg), and 4/8-byte
+// copies (.ca; .cg only exists for 16 bytes).
+__device__ __forceinline__ void cp_async_16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(smem)),
+               "l"(gmem));
+}
+template <int N>
+__device__ __forceinline__ void cp_async_small(void* smem, const void* gmem) {
+  static_assert(N == 4 || N == 8 || N == 16, "cp.async size");
+  if constexpr (N == 16) {
+    cp_async_16(smem, gmem);
+  } else {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;\n" ::"r"(smem_addr(smem)),
+                 "l"(gmem), "n"(N));
+  }
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::);
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// Four packed bytes (8 e2m1 codes) -> four f16x2: h[j] holds byte j, its low
+// nibble (the even element) in the low half.
+__device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n"
+      " .reg .b8 b0, b1, b2, b3;\n"
+      " mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+      " cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n"
+      " cvt.rn.f16x2.e2m1x2 %3, b3;\n"
+      "}\n"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+// Two E4M3 bytes (low byte -> low half) -> f16x2.  Every E4M3 value is exact
+// in f16 (range 2^-9 .. 448, 4 significant bits).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+  uint32_t r;
+  unsigned short in = static_cast<unsigned short>(two_bytes & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(in));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// {lo: a.lo, hi: b.lo} and {lo: a.hi, hi: b.hi}
+__device__ __forceinline__ uint32_t pack_lo(uint32_t a, uint32_t b) {
+  return __byte_perm(a, b, 0x5410);
+}
+__device__ __forceinline__ uint32_t pack_hi(uint32_t a, uint32_t b) {
+  return __byte_perm(a, b, 0x7632);
+}
+// broadcast a half: {x.lo, x.lo} / {x.hi, x.hi}
+__device__ __forceinline__ uint32_t bcast_lo(uint32_t x) {
+  return __byte_perm(x, x, 0x1010);
+}
+__device__ __forceinline__ uint32_t bcast_hi(uint32_t x) {
+  return __byte_perm(x, x, 0x3232);
+}
+
+// Two f32 -> f16x2 (round to nearest even), lo from a.
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+
+// D += A * B, m16n8k16, f16 inputs, f32 accumulators.
+//   A (row-major 16x16): a[0]={A[g][2t],A[g][2t+1]}, a[1]=rows g+8,
+//                        a[2]=cols 2t+8.., a[3]=rows g+8, cols 2t+8..
+//   B (col-major 16x8):  b[0]={B[2t][g],B[2t+1][g]}, b[1]=rows 2t+8..
+//   D (16x8):            d[0]=D[g][2t], d[1]=D[g][2t+1], d[2]/d[3]=row g+8
+// with g = lane/4, t = lane%4.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
+                                          uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// 2^x by the hardware approximation (PTX ex2.approx.ftz.f32).
+__device__ __forceinline__ float ex2(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;\n" : "=h"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
+  return __uint_as_float(bits16 << 16);
+}
+
+}  // namespace dev
+}  // namespace nvfp4kv

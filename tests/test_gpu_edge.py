@@ -1,0 +1,192 @@
+"""GPU edge cases against the oracle: ragged and tiny lengths, empty query
+sets, every head-dim pair and GQA group size, NHD / HND / padded layouts and
+independent K/V stride families, page-order invariance with poisoned unused
+pages, the pages' uniform-score probes, device-side index checks, and the
+standalone merge."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gpu_harness as H
+import oracle as O
+import nvfp4_paged_kv_nvfp4kv_gb300 as N
+from nvfp4_paged_kv_nvfp4kv_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def small(**kw):
+    args = dict(seed=21, kv_lens=(1, 16, 17, 31, 33, 250), qo_len=1, num_qo_heads=8,
+                num_kv_heads=2, head_dim_qk=128, head_dim_vo=128)
+    args.update(kw)
+    args["batch"] = len(args["kv_lens"])
+    return W.make_batch(W.custom_workload(**args))
+
+
+def check(batch, layout="HND", **plan_kw):
+    g = H.GpuCase(batch, layout=layout, **plan_kw)
+    oc, pt = H.oracle_cache(batch, layout)
+    H.compare_cache_bytes(g.cache, oc)
+    out, lse = g.run()
+    ro, rl = H.oracle_attention(batch, oc, pt)
+    return H.compare(out, lse, ro, rl), g, (out, lse)
+
+
+@pytest.mark.parametrize("layout", ["HND", "NHD"])
+@pytest.mark.parametrize("split", [False, True])
+def test_ragged_lengths(layout, split):
+    kw = dict(force_chunk_tokens=32) if split else dict(disable_split=True)
+    check(small(), layout, **kw)
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (256, 256), (256, 128), (512, 256)])
+def test_head_dims(dk, dv):
+    check(small(head_dim_qk=dk, head_dim_vo=dv, kv_lens=(5, 40, 300)), force_chunk_tokens=64)
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 1), (16, 2), (32, 1), (12, 4)])
+def test_group_sizes(hq, hkv):
+    check(small(num_qo_heads=hq, num_kv_heads=hkv, kv_lens=(3, 77, 129)))
+
+
+@pytest.mark.parametrize("qo_len", [2, 5, 16])
+def test_causal_extend(qo_len):
+    check(small(qo_len=qo_len, causal=True, kv_lens=(16, 40, 161)), force_chunk_tokens=32)
+
+
+def test_extend_all_tokens_new_and_shared_prefix():
+    batch = small(qo_len=16, causal=True, kv_lens=(16, 80, 1100, 2000),
+                  shared_prefix_tokens=0)
+    check(batch)
+    batch2 = small(qo_len=8, causal=True, kv_lens=(1030, 1100, 1500), shared_prefix_tokens=1024)
+    check(batch2)
+
+
+def test_requests_without_queries():
+    batch = small(kv_lens=(20, 50, 70, 90), qo_len=2, causal=True)
+    # requests 0 and 2 ask no query rows; 1 and 3 keep theirs
+    keep = torch.tensor([2, 3, 6, 7])
+    batch.q = batch.q[keep].contiguous()
+    batch.qo_indptr = torch.tensor([0, 0, 2, 2, 4], dtype=torch.int32)
+    check(batch)
+    check(batch, force_chunk_tokens=16)
+
+
+def test_padded_pages_and_independent_kv_strides():
+    batch = small(kv_lens=(37, 100, 260))
+    check(batch, "HND", pad_page_bytes=48)
+    # K pool HND, V pool NHD with padding: separate stride families
+    g = H.GpuCase(batch, append=False)
+    lay_v = batch.cache_layout("NHD", pad_page_bytes=96)
+    for w in ("v_data", "v_sf"):
+        n = lay_v.nbytes(w)
+        setattr(g.cache, w, torch.zeros(n, dtype=torch.uint8, device="cuda"))
+        g.cache.strides[w] = lay_v.strides(lay_v.rows()[w])
+    g.append(batch.prefix)
+    g.append(batch.new)
+    oc, pt = H.oracle_cache(batch, "HND")
+    out, lse = g.run()
+    ro, rl = H.oracle_attention(batch, oc, pt)
+    H.compare(out, lse, ro, rl)
+
+
+def test_page_order_invariance_with_poison():
+    batch = small(kv_lens=(37, 100, 260))
+    b1 = W.make_batch(batch.cfg, extra_pages=7)
+    g1 = H.GpuCase(b1, fill=0xFF, force_chunk_tokens=48)
+    o1, l1 = g1.run()
+    perm = torch.randperm(b1.num_pages, generator=torch.Generator().manual_seed(3))
+    b1.kv_indices = perm[b1.kv_indices.long()].to(torch.int32)
+    g2 = H.GpuCase(b1, fill=0xFF, force_chunk_tokens=48)
+    o2, l2 = g2.run()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
+    assert not torch.isnan(o1.float()).any()
+
+
+def test_v_ones_probe_exact():
+    # uniform-score / V = ones probe (page "fix(attention): correct SM120
+    # NVFP4 ... lse"): the output is the dequantised value of 1, 1.03125
+    batch = small(kv_lens=(37, 100, 250), qo_len=3, causal=True)
+    for ts in (batch.prefix, batch.new):
+        ts.v.fill_(1.0)
+    g = H.GpuCase(batch)
+    out, _ = g.run()
+    assert torch.all(out.float() == 1.03125)
+
+
+def test_q_zero_probe_lse_is_ln_len():
+    batch = small(kv_lens=(1, 37, 100, 250))
+    batch.q.zero_()
+    g = H.GpuCase(batch, force_chunk_tokens=32)
+    out, lse = g.run()
+    want = torch.tensor([math.log(L) for L in batch.kv_lens], device="cuda")
+    assert torch.allclose(lse, want[:, None].expand_as(lse), atol=1e-5, rtol=0)
+    oc, pt = H.oracle_cache(batch)
+    ro, rl = H.oracle_attention(batch, oc, pt)
+    H.compare(out, lse, ro, rl)
+
+
+def test_bad_page_index_sets_flag_without_fault():
+    batch = small(kv_lens=(37, 100))
+    g = H.GpuCase(batch)
+    assert N.nvfp4kv_workspace_flags(g.plan, clear=True) == 0
+    bad = g.kv_indices.clone()
+    bad[1] = batch.num_pages + 5
+    out = torch.empty((2, 8, 128), dtype=torch.bfloat16, device="cuda")
+    N.nvfp4kv_decode_run(g.plan, g.q, g.cache, bad, batch.sm_scale, out=out)
+    torch.cuda.synchronize()
+    assert N.nvfp4kv_workspace_flags(g.plan, clear=True) & 0x1
+    out2, _ = g.run()  # the context still works and the good table is clean
+    assert N.nvfp4kv_workspace_flags(g.plan) == 0
+    assert not torch.isnan(out2.float()).any()
+
+
+def test_append_out_of_range_sets_flag_and_writes_nothing():
+    batch = small(kv_lens=(37, 100))
+    g = H.GpuCase(batch, append=False)
+    before = g.cache.k_data.clone()
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k = batch.new.k[:1].cuda()
+    v = batch.new.v[:1].cuda()
+    for b, pos in ((0, 37), (5, 0), (1, -1)):
+        N.nvfp4kv_quantize_append(g.cache, k, v, H.dev_i32([b]), H.dev_i32([pos]),
+                                  g.kv_indices, g.kv_indptr, g.last, device_flags=flags)
+    torch.cuda.synchronize()
+    assert int(flags.item()) & 0x2
+    assert torch.equal(before, g.cache.k_data)
+
+
+def test_merge_states_matches_oracle():
+    rng = np.random.default_rng(5)
+    counts = [1, 2, 3, 17, 40, 1, 5]
+    P = sum(counts)
+    o = rng.standard_normal((P, 128)).astype(np.float32)
+    l = (rng.standard_normal(P) * 4).astype(np.float32)
+    l[3:6] = -np.inf                     # entry 2 fully masked
+    l[40] = -np.inf                      # one masked partial inside entry 4
+    indptr = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    out, lse = N.nvfp4kv_merge_states(torch.from_numpy(o).cuda(), torch.from_numpy(l).cuda(),
+                                      torch.from_numpy(indptr).cuda())
+    torch.cuda.synchronize()
+    for e in range(len(counts)):
+        a, b = indptr[e], indptr[e + 1]
+        ro, rl = O.merge_states(o[a:b].astype(np.float64), l[a:b].astype(np.float64))
+        if rl == -math.inf:
+            assert float(lse[e]) == -math.inf and torch.all(out[e] == 0)
+            continue
+        assert abs(float(lse[e]) - rl) <= 1e-5
+        assert np.abs(out[e].float().cpu().numpy() - ro).max() <= 1e-2 * max(1, np.abs(ro).max())
+
+
+def test_lse_optional():
+    batch = small(kv_lens=(37, 100))
+    g = H.GpuCase(batch)
+    out = torch.empty((2, 8, 128), dtype=torch.bfloat16, device="cuda")
+    N.nvfp4kv_decode_run(g.plan, g.q, g.cache, g.kv_indices, batch.sm_scale, out=out,
+                         lse=None)
+    torch.cuda.synchronize()
+    ref, _ = g.run()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))

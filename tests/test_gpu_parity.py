@@ -1,0 +1,86 @@
+"""GPU parity of the CUDA path (through the C ABI) against the float64 oracle
+on the five benchmark workloads at their full sizes: the quantiser must be
+byte-identical, attention within max-abs 5e-3 (out) and 1e-3 (lse), no NaN,
+lse written for every row.  The prefix-cache extend workload is checked on
+three sampled requests (shortest, median, longest) because the oracle takes
+minutes on all 32."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_harness as H
+from nvfp4_paged_kv_nvfp4kv_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+_cases = {}
+
+
+def case(name):
+    if name not in _cases:
+        batch = W.make_batch(W.WORKLOADS[name])
+        g = H.GpuCase(batch)
+        requests = None
+        if name == "prefix_cache_extend":
+            order = np.argsort(batch.kv_lens)
+            requests = sorted({int(order[0]), int(order[len(order) // 2]), int(order[-1])})
+        oc, pt = H.oracle_cache(batch, requests=requests)
+        _cases[name] = (batch, g, oc, pt, requests)
+    return _cases[name]
+
+
+@pytest.mark.parametrize("name", list(W.WORKLOADS))
+def test_quantize_append_bit_exact(name):
+    batch, g, oc, pt, requests = case(name)
+    assert int(g.flags.item()) == 0
+    pages = None
+    if requests is not None:
+        kvp = batch.kv_indptr.tolist()
+        pages = sorted({int(batch.kv_indices[i]) for b in requests
+                        for i in range(kvp[b], kvp[b + 1])})
+    H.compare_cache_bytes(g.cache, oc, pages)
+
+
+@pytest.mark.parametrize("name", list(W.WORKLOADS))
+def test_attention_parity(name):
+    batch, g, oc, pt, requests = case(name)
+    out, lse = g.run()
+    ro, rl = H.oracle_attention(batch, oc, pt, requests)
+    stats = H.compare(out, lse, ro, rl)
+    print(name, "split=%d units=%d" % (g.plan.info.split, g.plan.info.num_units), stats)
+    if requests is None:  # every row written
+        assert not torch.isnan(lse).any() and not torch.isnan(out.float()).any()
+    if name == "long_context_decode":
+        assert g.plan.info.split == 1
+
+
+def test_split_and_unsplit_agree():
+    batch, g, oc, pt, _ = case("long_context_decode")
+    assert g.plan.info.split == 1
+    o_split, l_split = g.run()
+    c = batch.cfg
+    p1 = H.N.nvfp4kv_decode_plan(batch.qo_indptr, batch.kv_indptr, batch.last_page_len,
+                                 c.num_qo_heads, c.num_kv_heads, c.head_dim_qk,
+                                 c.head_dim_vo, disable_split=True)
+    assert p1.info.split == 0
+    o_un, l_un = g.run(p1)
+    a, b = o_split.float(), o_un.float()
+    ulp = torch.clamp(b.abs(), min=2 ** -126)
+    ulp = 2.0 ** (torch.floor(torch.log2(ulp)) - 7)
+    diff = (a - b).abs()
+    assert bool((diff <= torch.maximum(torch.full_like(diff, 5e-4), 2 * ulp)).all())
+    assert float((l_split - l_un).abs().max()) <= 1e-4
+
+
+@pytest.mark.parametrize("chunk", [16, 32, 48, 1024, 2048])
+def test_forced_chunk_sweep(chunk):
+    batch, g, oc, pt, _ = case("long_context_decode")
+    c = batch.cfg
+    p = H.N.nvfp4kv_decode_plan(batch.qo_indptr, batch.kv_indptr, batch.last_page_len,
+                                c.num_qo_heads, c.num_kv_heads, c.head_dim_qk,
+                                c.head_dim_vo, force_chunk_tokens=chunk)
+    assert p.info.chunk_pages == chunk // 16 and p.info.split == 1
+    out, lse = g.run(p)
+    ro, rl = H.oracle_attention(batch, oc, pt) if "ref" not in _cases else _cases["ref"]
+    _cases["ref"] = (ro, rl)
+    H.compare(out, lse, ro, rl)
