@@ -269,14 +269,14 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
   const int32_t total_rows = batch > 0 ? qo_indptr_h[batch] : 0;
 
   // ---- kernel choice and occupancy --------------------------------------
-  const int rows_per_block = max_rows <= 8 ? 8 : 16;
   int kind = opts.kernel;
   AttendConfig cfg{};
   if (kind == 0) kind = kKernelTensorCore;
-  if (!lookup_kernel(kind, head_dim_qk, head_dim_vo, rows_per_block, &cfg))
+  if (!lookup_kernel(kind, head_dim_qk, head_dim_vo, max_rows <= 8 ? 8 : 16, &cfg))
     return fail(NVFP4KV_ERR_UNSUPPORTED, "no %s kernel for head dims (%d, %d)",
                 kind == kKernelTensorCore ? "tensor-core" : "CUDA-core", head_dim_qk,
                 head_dim_vo);
+  const int rows_per_block = cfg.rows;
   int num_sms = opts.num_sms, ctas_per_sm = opts.ctas_per_sm;
   if (num_sms == 0 || ctas_per_sm == 0) {
     int dev = device;

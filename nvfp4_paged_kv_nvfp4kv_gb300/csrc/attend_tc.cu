@@ -40,6 +40,7 @@
 
 #include "device_common.cuh"
 #include "internal.h"
+#include "stage.cuh"
 
 namespace nvfp4kv {
 namespace {
@@ -47,78 +48,24 @@ namespace {
 using namespace dev;
 
 template <int DK, int DV, int NT, int WARPS, int STAGES>
-struct TcTraits {
+struct TcTraits : PageStage<DK, DV> {
+  using S = PageStage<DK, DV>;
   static constexpr int RB = 8 * NT;                  // query rows per CTA
   static constexpr int CB = (DK / 8 < 16) ? DK / 8 : 16;  // K bytes per lane chunk
   static constexpr int NCH = (DK / 8) / CB;          // K chunks per lane
   static constexpr int KSTEPS = DK / 16;
   static constexpr int KS_PER_CH = CB / 2;
-  static constexpr int KROW = DK / 2;                // smem row of packed K
-  static constexpr bool KSWZ = DK >= 256;            // xor-swizzle odd rows
-  static constexpr int KSFROW = DK / 16;
   static constexpr int VC = DV / 16;                 // V bytes per lane per token
-  // padded V row: the PV reads (lane group g, tokens 2t..) hit distinct banks
-  static constexpr int VROW = DV / 2 + 16;
-  static constexpr int VSFROW = DV / 16;
   static constexpr int MT = DV / 16;                 // PV m-tiles
-  static constexpr int K_BYTES = 16 * KROW;
-  static constexpr int KSF_BYTES = 16 * KSFROW;
-  static constexpr int V_BYTES = 16 * VROW;
-  static constexpr int VSF_BYTES = 16 * VSFROW;
-  static constexpr int OFF_KSF = K_BYTES;
-  static constexpr int OFF_V = (OFF_KSF + KSF_BYTES + 15) / 16 * 16;
-  static constexpr int OFF_VSF = OFF_V + V_BYTES;
-  static constexpr int STAGE_BYTES = (OFF_VSF + VSF_BYTES + 15) / 16 * 16;
-  static constexpr int PIPE_BYTES = WARPS * STAGES * STAGE_BYTES;
+  static constexpr int PIPE_BYTES = WARPS * STAGES * S::STAGE_BYTES;
   static constexpr int COMB_BYTES = WARPS * RB * (DV + 2) * 4;
   static constexpr int MAIN_BYTES = PIPE_BYTES > COMB_BYTES ? PIPE_BYTES : COMB_BYTES;
   static constexpr int QROW = DK + 8;                // f16 elements, padded
   static constexpr int Q_BYTES = RB * QROW * 2;
   static constexpr int SMEM = MAIN_BYTES + Q_BYTES + RB * 16;
   static constexpr bool Q_IN_REGS = KSTEPS * 2 * NT <= 32;
-  static_assert(DK % 64 == 0 && DV % 64 == 0, "head dims");
-  static_assert(VROW % 16 == 0, "V rows must stay 16-byte aligned");
+  static_assert(S::VC == VC, "V lane chunk");
 };
-
-// Copy one page (16 tokens of one kv head) into a warp's stage.
-template <class T>
-__device__ __forceinline__ void issue_page(uint8_t* st, const CacheView& c,
-                                           int32_t pid, int h, int lane) {
-  const uint8_t* kb = c.k_data + pid * c.k_sp + h * c.k_sh;
-  const uint8_t* vb = c.v_data + pid * c.v_sp + h * c.v_sh;
-  const uint8_t* ksb = c.k_sf + pid * c.ksf_sp + h * c.ksf_sh;
-  const uint8_t* vsb = c.v_sf + pid * c.vsf_sp + h * c.vsf_sh;
-  constexpr int KCH = T::KROW / 16;      // 16-byte chunks per K row
-  constexpr int VCHR = (T::VC * 8) / 16;  // 16-byte chunks per V row (DV/32)
-#pragma unroll
-  for (int ci = lane; ci < 16 * KCH; ci += 32) {
-    const int r = ci / KCH, ch = ci % KCH;
-    const int pos = T::KSWZ ? (ch ^ ((r & 1) << 2)) : ch;
-    cp_async_16(st + r * T::KROW + pos * 16, kb + r * c.k_ss + ch * 16);
-  }
-#pragma unroll
-  for (int ci = lane; ci < 16 * VCHR; ci += 32) {
-    const int r = ci / VCHR, ch = ci % VCHR;
-    cp_async_16(st + T::OFF_V + r * T::VROW + ch * 16, vb + r * c.v_ss + ch * 16);
-  }
-  // scale rows: KSFROW bytes per token, copied in units of min(16, KSFROW)
-  constexpr int KSU = T::KSFROW < 16 ? T::KSFROW : 16;
-  constexpr int KSN = T::KSFROW / KSU;
-#pragma unroll
-  for (int ci = lane; ci < 16 * KSN; ci += 32) {
-    const int r = ci / KSN, u = ci % KSN;
-    cp_async_small<KSU>(st + T::OFF_KSF + r * T::KSFROW + u * KSU,
-                        ksb + r * c.ksf_ss + u * KSU);
-  }
-  constexpr int VSU = T::VSFROW < 16 ? T::VSFROW : 16;
-  constexpr int VSN = T::VSFROW / VSU;
-#pragma unroll
-  for (int ci = lane; ci < 16 * VSN; ci += 32) {
-    const int r = ci / VSN, u = ci % VSN;
-    cp_async_small<VSU>(st + T::OFF_VSF + r * T::VSFROW + u * VSU,
-                        vsb + r * c.vsf_ss + u * VSU);
-  }
-}
 
 template <int DK, int DV, int NT, int WARPS, int STAGES>
 __global__ void __launch_bounds__(WARPS * 32)
@@ -233,7 +180,8 @@ __global__ void __launch_bounds__(WARPS * 32)
       if (lane == 0) atomicOr(p.flags, 0x1u);
       pid = 0;
     }
-    issue_page<T>(wpipe + (i % STAGES) * T::STAGE_BYTES, p.cache, pid, u.h_kv, lane);
+    issue_page<typename T::S>(wpipe + (i % STAGES) * T::STAGE_BYTES, p.cache, pid, u.h_kv,
+                              lane);
   };
 
 #pragma unroll
@@ -265,7 +213,7 @@ __global__ void __launch_bounds__(WARPS * 32)
         uint32_t w[T::CB / 4];
         uint32_t sc0, sc1;
         if constexpr (T::CB == 16) {
-          const int pos = T::KSWZ ? (ch ^ ((row & 1) << 2)) : ch;
+          const int pos = T::S::k_pos(row, ch);
           const uint4 v = *reinterpret_cast<const uint4*>(st + row * T::KROW + pos * 16);
           w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
           const uint32_t sfp = *reinterpret_cast<const uint16_t*>(

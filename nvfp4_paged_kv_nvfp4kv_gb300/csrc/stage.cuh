@@ -1,0 +1,80 @@
+// stage.cuh -- shared-memory stage of one page (16 tokens of one kv head)
+// and the cp.async copies that fill it; shared by the attention kernels.
+#pragma once
+
+#include <cstdint>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace nvfp4kv {
+
+// Stage layout: packed K rows [16][Dk/2] (odd rows xor-swizzled by 4 chunks
+// when Dk >= 256 so a lane quad's 16-byte reads of two rows hit different
+// banks), K scale rows [16][Dk/16], packed V rows [16][Dv/2 + 16] (padded so
+// the PV reads of lane group g at tokens 2t.. hit distinct banks), V scale
+// rows [16][Dv/16].  Every section starts 16-byte aligned.
+template <int DK, int DV>
+struct PageStage {
+  static constexpr int KROW = DK / 2;
+  static constexpr bool KSWZ = DK >= 256;
+  static constexpr int KSFROW = DK / 16;
+  static constexpr int VC = DV / 16;
+  static constexpr int VROW = DV / 2 + 16;
+  static constexpr int VSFROW = DV / 16;
+  static constexpr int K_BYTES = 16 * KROW;
+  static constexpr int KSF_BYTES = 16 * KSFROW;
+  static constexpr int V_BYTES = 16 * VROW;
+  static constexpr int VSF_BYTES = 16 * VSFROW;
+  static constexpr int OFF_KSF = K_BYTES;
+  static constexpr int OFF_V = (OFF_KSF + KSF_BYTES + 15) / 16 * 16;
+  static constexpr int OFF_VSF = OFF_V + V_BYTES;
+  static constexpr int STAGE_BYTES = (OFF_VSF + VSF_BYTES + 15) / 16 * 16;
+  static_assert(DK % 64 == 0 && DV % 64 == 0, "head dims");
+  static_assert(VROW % 16 == 0, "V rows must stay 16-byte aligned");
+
+  __device__ static __forceinline__ int k_pos(int row, int chunk) {
+    return KSWZ ? (chunk ^ ((row & 1) << 2)) : chunk;
+  }
+};
+
+// Copy one page (16 tokens of kv head h, page id pid) into a warp's stage.
+template <class S>
+__device__ __forceinline__ void issue_page(uint8_t* st, const CacheView& c, int32_t pid,
+                                           int h, int lane) {
+  using namespace dev;
+  const uint8_t* kb = c.k_data + pid * c.k_sp + h * c.k_sh;
+  const uint8_t* vb = c.v_data + pid * c.v_sp + h * c.v_sh;
+  const uint8_t* ksb = c.k_sf + pid * c.ksf_sp + h * c.ksf_sh;
+  const uint8_t* vsb = c.v_sf + pid * c.vsf_sp + h * c.vsf_sh;
+  constexpr int KCH = S::KROW / 16;       // 16-byte chunks per K row
+  constexpr int VCHR = (S::VC * 8) / 16;  // 16-byte chunks per V row
+#pragma unroll
+  for (int ci = lane; ci < 16 * KCH; ci += 32) {
+    const int r = ci / KCH, ch = ci % KCH;
+    cp_async_16(st + r * S::KROW + S::k_pos(r, ch) * 16, kb + r * c.k_ss + ch * 16);
+  }
+#pragma unroll
+  for (int ci = lane; ci < 16 * VCHR; ci += 32) {
+    const int r = ci / VCHR, ch = ci % VCHR;
+    cp_async_16(st + S::OFF_V + r * S::VROW + ch * 16, vb + r * c.v_ss + ch * 16);
+  }
+  constexpr int KSU = S::KSFROW < 16 ? S::KSFROW : 16;
+  constexpr int KSN = S::KSFROW / KSU;
+#pragma unroll
+  for (int ci = lane; ci < 16 * KSN; ci += 32) {
+    const int r = ci / KSN, u = ci % KSN;
+    cp_async_small<KSU>(st + S::OFF_KSF + r * S::KSFROW + u * KSU,
+                        ksb + r * c.ksf_ss + u * KSU);
+  }
+  constexpr int VSU = S::VSFROW < 16 ? S::VSFROW : 16;
+  constexpr int VSN = S::VSFROW / VSU;
+#pragma unroll
+  for (int ci = lane; ci < 16 * VSN; ci += 32) {
+    const int r = ci / VSN, u = ci % VSN;
+    cp_async_small<VSU>(st + S::OFF_VSF + r * S::VSFROW + u * VSU,
+                        vsb + r * c.vsf_ss + u * VSU);
+  }
+}
+
+}  // namespace nvfp4kv

@@ -190,3 +190,13 @@ def test_lse_optional():
     torch.cuda.synchronize()
     ref, _ = g.run()
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (256, 128), (512, 256)])
+@pytest.mark.parametrize("causal,qo_len", [(False, 1), (True, 4)])
+def test_cuda_core_kernel(dk, dv, causal, qo_len):
+    batch = small(head_dim_qk=dk, head_dim_vo=dv, kv_lens=(5, 40, 300), qo_len=qo_len,
+                  causal=causal)
+    stats, g, _ = check(batch, kernel=2, force_chunk_tokens=64)
+    assert g.plan.info.kernel == 2 and g.plan.info.rows_per_block == 8
+    stats2, g2, _ = check(batch, kernel=2, disable_split=True)
