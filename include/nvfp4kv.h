@@ -162,6 +162,7 @@ typedef struct nvfp4kv_plan_info {
   uint64_t plan_host_bytes;  /* host bytes the plan writes into plan_host    */
   uint64_t off_flags, off_units, off_merge_indptr, off_partial_lse,
       off_partial_o;       /* byte offsets inside the workspace              */
+  uint64_t off_counters;   /* merge arrival counters (self-resetting)        */
 } nvfp4kv_plan_info;
 
 /* Build the plan from HOST copies of the batch description.
@@ -192,8 +193,13 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
 
 /* ---- run ------------------------------------------------------------------ */
 /* Attention for the planned batch: GQA-grouped QK^T, online softmax and PV
- * over the dequantised pages, then (when the plan split the work) the
- * log-sum-exp merge.  Calls only kernels: it can be captured in a CUDA graph.
+ * over the dequantised pages.  When the plan split a request, every work unit
+ * stores an f32 partial (o, lse) in the workspace and the last unit of each
+ * (request, kv head, row block) to finish folds them by log-sum-exp (the merge
+ * of nvfp4kv_merge_states) into out/lse; units find out who is last through
+ * counters in the workspace and never wait for one another.  One kernel
+ * launch; nothing else is enqueued, so the call can be captured in a CUDA
+ * graph.  One workspace must not be used by two runs in flight at once.
  *   q_bf16 [dev]  element (row, head, d) at q[row*q_stride_tok +
  *                 head*q_stride_head + d]; strides in elements, multiples
  *                 of 8; 16-byte aligned.
@@ -211,16 +217,16 @@ int nvfp4kv_decode_run(const nvfp4kv_plan_info* info, const void* q_bf16,
                        void* workspace, uint64_t workspace_bytes,
                        void* out_bf16, float* lse, cudaStream_t stream);
 
-/* The two halves of nvfp4kv_decode_run, for callers that time or overlap
- * them: the attention kernel (writes out/lse directly when the plan has no
- * split, partial states into the workspace otherwise) and the merge of the
- * plan's partial states (a no-op without split). */
+/* Same as nvfp4kv_decode_run (kept as the name of the attention half). */
 int nvfp4kv_decode_attend(const nvfp4kv_plan_info* info, const void* q_bf16,
                           int64_t q_stride_tok, int64_t q_stride_head,
                           const nvfp4kv_paged_cache* cache,
                           const int32_t* kv_indices, float sm_scale,
                           void* workspace, uint64_t workspace_bytes,
                           void* out_bf16, float* lse, cudaStream_t stream);
+/* Re-merge the partial states a split run left in the workspace with the
+ * standalone merge kernel (nvfp4kv_merge_states over the plan's merge
+ * indptr); rewrites out/lse with the same values.  A no-op without split. */
 int nvfp4kv_decode_merge(const nvfp4kv_plan_info* info, void* workspace,
                          uint64_t workspace_bytes, void* out_bf16, float* lse,
                          cudaStream_t stream);

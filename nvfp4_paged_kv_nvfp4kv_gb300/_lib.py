@@ -55,7 +55,7 @@ class PlanInfo(C.Structure):
         ("num_partials", C.c_int64), ("total_kv_pages", C.c_int64)] + [
         (n, C.c_uint64) for n in (
             "workspace_bytes", "plan_host_bytes", "off_flags", "off_units",
-            "off_merge_indptr", "off_partial_lse", "off_partial_o")]
+            "off_merge_indptr", "off_partial_lse", "off_partial_o", "off_counters")]
 
 
 _vp, _i32, _i64, _u64, _f32 = C.c_void_p, C.c_int32, C.c_int64, C.c_uint64, C.c_float

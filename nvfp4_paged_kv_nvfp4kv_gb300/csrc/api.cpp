@@ -372,6 +372,7 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
         u.split = s;
         u.num_splits = S;
         u.partial_base = static_cast<int32_t>(pbase[b]);
+        u.pair = b * num_kv_heads + h;
         units.push_back(u);
       }
   }
@@ -390,7 +391,9 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
 
   // ---- layout ------------------------------------------------------------
   const uint64_t off_flags = 0;
-  const uint64_t off_units = 256;
+  const uint64_t off_counters = 256;
+  const uint64_t n_counters = split ? (uint64_t)batch * num_kv_heads * row_blocks : 0;
+  const uint64_t off_units = align_up(off_counters + n_counters * 4, 256);
   const uint64_t off_merge = align_up(off_units + units.size() * sizeof(WorkUnit), 256);
   const uint64_t off_plse = align_up(off_merge + (split ? (entries + 1) * 4 : 0), 256);
   const uint64_t off_po = align_up(off_plse + partial * 4, 256);
@@ -426,6 +429,7 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
   info->off_merge_indptr = off_merge;
   info->off_partial_lse = off_plse;
   info->off_partial_o = off_po;
+  info->off_counters = off_counters;
 
   if (host_bytes > 0 && (!plan_host || plan_host_bytes < host_bytes))
     return fail(NVFP4KV_ERR_WORKSPACE_TOO_SMALL, "plan_host needs %llu bytes",
@@ -454,7 +458,7 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
   if (host_bytes > 0)
     e = cudaMemcpyAsync(ws + off_units, hb, host_bytes, cudaMemcpyHostToDevice, stream);
   if (e != cudaSuccess) return cuda_fail(e, "plan upload");
-  e = cudaMemsetAsync(ws + off_flags, 0, 4, stream);
+  e = cudaMemsetAsync(ws + off_flags, 0, off_units - off_flags, stream);  // flags, counters
   if (e != cudaSuccess) return cuda_fail(e, "flag reset");
   return ok();
 }
@@ -523,6 +527,7 @@ int nvfp4kv_decode_attend(const nvfp4kv_plan_info* info, const void* q_bf16,
   p.lse = lse;
   p.partial_o = reinterpret_cast<float*>(ws + info->off_partial_o);
   p.partial_lse = reinterpret_cast<float*>(ws + info->off_partial_lse);
+  p.counters = reinterpret_cast<int*>(ws + info->off_counters);
   p.flags = reinterpret_cast<uint32_t*>(ws + info->off_flags);
   e = launch_attend(cfg, p, info->num_units, info->row_blocks, stream);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
@@ -555,11 +560,9 @@ int nvfp4kv_decode_run(const nvfp4kv_plan_info* info, const void* q_bf16,
                        const nvfp4kv_paged_cache* cache, const int32_t* kv_indices,
                        float sm_scale, void* workspace, uint64_t workspace_bytes,
                        void* out_bf16, float* lse, cudaStream_t stream) {
-  int st = nvfp4kv_decode_attend(info, q_bf16, q_stride_tok, q_stride_head, cache,
-                                 kv_indices, sm_scale, workspace, workspace_bytes, out_bf16,
-                                 lse, stream);
-  if (st) return st;
-  return nvfp4kv_decode_merge(info, workspace, workspace_bytes, out_bf16, lse, stream);
+  // the split-KV merge is fused into the attention kernel
+  return nvfp4kv_decode_attend(info, q_bf16, q_stride_tok, q_stride_head, cache, kv_indices,
+                               sm_scale, workspace, workspace_bytes, out_bf16, lse, stream);
 }
 
 int nvfp4kv_merge_states(const float* o_partial, const float* lse_partial,

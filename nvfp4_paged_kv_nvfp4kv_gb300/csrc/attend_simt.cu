@@ -18,6 +18,7 @@
 
 #include "device_common.cuh"
 #include "internal.h"
+#include "epilogue.cuh"
 #include "stage.cuh"
 
 namespace nvfp4kv {
@@ -174,8 +175,10 @@ __global__ void __launch_bounds__(WARPS * 32) attend_simt_kernel(const AttendPar
       m_run[r] = m_new;
       pv[r] = ex2(x - m_use);
       l_run[r] = l_run[r] * corr + (half == 0 ? pv[r] : 0.f);
+      if (corr != 1.f) {  // warp-uniform: m is the same in every lane
 #pragma unroll
-      for (int k = 0; k < T::VD; ++k) o[r][k] *= corr;
+        for (int k = 0; k < T::VD; ++k) o[r][k] *= corr;
+      }
     }
     // p * (V block scale of the token for this lane's dims): lanes 0..15
     // write token `tok`'s factor; the lane's dims lie in one block
@@ -244,43 +247,8 @@ __global__ void __launch_bounds__(WARPS * 32) attend_simt_kernel(const AttendPar
 #pragma unroll
     for (int k = 0; k < T::VD; ++k) sO[(warp * RB + r) * DV + lane * T::VD + k] = o[r][k];
   __syncthreads();
-  const float kLn2 = 0.69314718055994530942f;
-  for (int idx = tid; idx < RB * (DV / 2); idx += WARPS * 32) {
-    const int rr = idx / (DV / 2), d = 2 * (idx % (DV / 2));
-    const int r = row0 + rr;
-    if (r >= R) continue;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < WARPS; ++w) M = fmaxf(M, sM[w * RB + rr]);
-    float L = 0.f, o0 = 0.f, o1 = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < WARPS; ++w) {
-        const float mw = sM[w * RB + rr];
-        const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-        L += sL[w * RB + rr] * sc;
-        o0 += sO[(w * RB + rr) * DV + d] * sc;
-        o1 += sO[(w * RB + rr) * DV + d + 1] * sc;
-      }
-      const float inv = p.v_scale / L;
-      o0 *= inv;
-      o1 *= inv;
-    }
-    const float lse_v = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
-    const int i = r / G, head = u.h_kv * G + r % G;
-    const int64_t qrow = u.qo_begin + i;
-    if (!p.split) {
-      const uint32_t packed =
-          (uint32_t)f32_to_bf16_bits(o0) | ((uint32_t)f32_to_bf16_bits(o1) << 16);
-      *reinterpret_cast<uint32_t*>(p.out + (qrow * Hq + head) * DV + d) = packed;
-      if (d == 0 && p.lse) p.lse[qrow * Hq + head] = lse_v;
-    } else {
-      const int64_t pi = (int64_t)u.partial_base +
-                         ((int64_t)i * Hq + head) * u.num_splits + u.split;
-      *reinterpret_cast<float2*>(p.partial_o + pi * DV + d) = make_float2(o0, o1);
-      if (d == 0) p.partial_lse[pi] = lse_v;
-    }
-  }
+  finish_unit<RB, DV, WARPS>(p, u, row0, R, sM, sL, sO,
+                            reinterpret_cast<float*>(sRowLim));
 }
 
 template <int DK, int DV>

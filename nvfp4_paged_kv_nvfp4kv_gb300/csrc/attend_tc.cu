@@ -40,6 +40,7 @@
 
 #include "device_common.cuh"
 #include "internal.h"
+#include "epilogue.cuh"
 #include "stage.cuh"
 
 namespace nvfp4kv {
@@ -281,7 +282,12 @@ __global__ void __launch_bounds__(WARPS * 32)
       pfrag[hf][0] = f32x2_to_f16x2(p0, p1);
       pfrag[hf][1] = f32x2_to_f16x2(p2, p3);
     }
-    // rescale O^T columns (query rows 8nq+2t, 8nq+2t+1)
+    // rescale O^T columns (query rows 8nq+2t, 8nq+2t+1); skipped when no
+    // row maximum of the warp moved (corr == 1 exactly for every row)
+    bool moved = false;
+#pragma unroll
+    for (int hf = 0; hf < NT; ++hf) moved |= corr[hf] != 1.f;
+    if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
     for (int nq = 0; nq < NT; ++nq) {
       const float cA = __shfl_sync(0xffffffffu, corr[nq], (2 * t) * 4);
@@ -293,6 +299,7 @@ __global__ void __launch_bounds__(WARPS * 32)
         oacc[mt][nq][2] *= cA;
         oacc[mt][nq][3] *= cB;
       }
+    }
     }
 
     // ---- O^T += V_hat^T P^T ---------------------------------------------
@@ -391,43 +398,7 @@ __global__ void __launch_bounds__(WARPS * 32)
   }
   __syncthreads();
 
-  const float kLn2 = 0.69314718055994530942f;
-  for (int idx = tid; idx < T::RB * (DV / 2); idx += WARPS * 32) {
-    const int rr = idx / (DV / 2), d = 2 * (idx % (DV / 2));
-    const int r = row0 + rr;
-    if (r >= R) continue;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < WARPS; ++w) M = fmaxf(M, sM[w * T::RB + rr]);
-    float L = 0.f, o0 = 0.f, o1 = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < WARPS; ++w) {
-        const float mw = sM[w * T::RB + rr];
-        const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-        L += sL[w * T::RB + rr] * sc;
-        const float2 ow = *reinterpret_cast<const float2*>(sO + (w * T::RB + rr) * DV + d);
-        o0 += ow.x * sc;
-        o1 += ow.y * sc;
-      }
-      const float inv = p.v_scale / L;
-      o0 *= inv;
-      o1 *= inv;
-    }
-    const float lse_v = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
-    const int i = r / G, head = u.h_kv * G + r % G;
-    const int64_t qrow = u.qo_begin + i;
-    if (!p.split) {
-      const uint32_t packed = (uint32_t)f32_to_bf16_bits(o0) | ((uint32_t)f32_to_bf16_bits(o1) << 16);
-      *reinterpret_cast<uint32_t*>(p.out + (qrow * Hq + head) * DV + d) = packed;
-      if (d == 0 && p.lse) p.lse[qrow * Hq + head] = lse_v;
-    } else {
-      const int64_t pi = (int64_t)u.partial_base +
-                         ((int64_t)i * Hq + head) * u.num_splits + u.split;
-      *reinterpret_cast<float2*>(p.partial_o + pi * DV + d) = make_float2(o0, o1);
-      if (d == 0) p.partial_lse[pi] = lse_v;
-    }
-  }
+  finish_unit<T::RB, DV, WARPS>(p, u, row0, R, sM, sL, sO, sRowF);
 }
 
 template <int DK, int DV, int NT>

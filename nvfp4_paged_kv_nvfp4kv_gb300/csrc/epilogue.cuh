@@ -1,0 +1,133 @@
+// epilogue.cuh -- end of an attention work unit: combine the warps' online-
+// softmax states of the CTA's query rows and store them; when the plan split
+// the request, store an f32 partial state and let the last CTA of the
+// (request, kv head, row block) fold all partials (log-sum-exp merge).
+//
+// The last CTA is found with a counter per (request, kv head, row block):
+// every CTA publishes its partials (__threadfence) and then increments the
+// counter; the CTA that sees num_splits - 1 is last, reads the partials
+// through L2 (ld.global.cg) and resets the counter to 0 for the next run.
+// No CTA waits for another.
+#pragma once
+
+#include <cstdint>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace nvfp4kv {
+
+// sM/sL: [WARPS][RB] running max (log2 domain) and sum of each warp;
+// sO: [WARPS][RB][DV] each warp's un-normalised output rows;
+// sFin: scratch of at least 2*RB floats + 1 int.
+template <int RB, int DV, int WARPS>
+__device__ __forceinline__ void finish_unit(const AttendParams& p, const WorkUnit& u,
+                                            int row0, int R, const float* sM,
+                                            const float* sL, const float* sO,
+                                            float* sFin) {
+  using namespace dev;
+  constexpr float kLn2 = 0.69314718055994530942f;
+  constexpr float kLog2e = 1.44269504088896340736f;
+  const int tid = threadIdx.x;
+  const int G = p.group, Hq = p.num_qo_heads;
+  const bool partial = p.split && u.num_splits > 1;
+
+  for (int idx = tid; idx < RB * (DV / 2); idx += WARPS * 32) {
+    const int rr = idx / (DV / 2), d = 2 * (idx % (DV / 2));
+    const int r = row0 + rr;
+    if (r >= R) continue;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) M = fmaxf(M, sM[w * RB + rr]);
+    float L = 0.f, o0 = 0.f, o1 = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < WARPS; ++w) {
+        const float mw = sM[w * RB + rr];
+        const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+        L += sL[w * RB + rr] * sc;
+        const float2 ow = *reinterpret_cast<const float2*>(sO + (w * RB + rr) * DV + d);
+        o0 += ow.x * sc;
+        o1 += ow.y * sc;
+      }
+      const float inv = p.v_scale / L;
+      o0 *= inv;
+      o1 *= inv;
+    }
+    const float lse_v = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
+    const int i = r / G, head = u.h_kv * G + r % G;
+    const int64_t qrow = u.qo_begin + i;
+    if (!partial) {
+      const uint32_t packed =
+          (uint32_t)f32_to_bf16_bits(o0) | ((uint32_t)f32_to_bf16_bits(o1) << 16);
+      *reinterpret_cast<uint32_t*>(p.out + (qrow * Hq + head) * DV + d) = packed;
+      if (d == 0 && p.lse) p.lse[qrow * Hq + head] = lse_v;
+    } else {
+      const int64_t pi = (int64_t)u.partial_base +
+                         ((int64_t)i * Hq + head) * u.num_splits + u.split;
+      *reinterpret_cast<float2*>(p.partial_o + pi * DV + d) = make_float2(o0, o1);
+      if (d == 0) p.partial_lse[pi] = lse_v;
+    }
+  }
+  if (!partial) return;
+
+  // ---- last CTA of the split group merges ------------------------------
+  int* s_last = reinterpret_cast<int*>(sFin + 2 * RB);
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    int* ctr = p.counters + (int64_t)u.pair * gridDim.y + blockIdx.y;
+    const int old = atomicAdd(ctr, 1);
+    *s_last = (old == u.num_splits - 1);
+    if (*s_last) *ctr = 0;  // every other CTA of the group has arrived
+  }
+  __syncthreads();
+  if (!*s_last) return;
+  __threadfence();
+  const int S = u.num_splits;
+  const int lane = tid & 31, warp = tid >> 5;
+  // per row: M = max lse_s, Lf = M + ln sum exp(lse_s - M)  (natural log)
+  for (int rr = warp; rr < RB; rr += WARPS) {
+    const int r = row0 + rr;
+    if (r >= R) continue;
+    const int i = r / G, head = u.h_kv * G + r % G;
+    const float* lp = p.partial_lse + (int64_t)u.partial_base +
+                      ((int64_t)i * Hq + head) * S;
+    float M = -INFINITY;
+    for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldcg(lp + s));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float sum = 0.f;
+    if (M != -INFINITY)
+      for (int s = lane; s < S; s += 32) sum += ex2((__ldcg(lp + s) - M) * kLog2e);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) sFin[rr] = (M == -INFINITY) ? -INFINITY : M + logf(sum);
+  }
+  __syncthreads();
+  for (int idx = tid; idx < RB * (DV / 2); idx += WARPS * 32) {
+    const int rr = idx / (DV / 2), d = 2 * (idx % (DV / 2));
+    const int r = row0 + rr;
+    if (r >= R) continue;
+    const int i = r / G, head = u.h_kv * G + r % G;
+    const int64_t base = (int64_t)u.partial_base + ((int64_t)i * Hq + head) * S;
+    const float Lf = sFin[rr];
+    float o0 = 0.f, o1 = 0.f;
+    if (Lf != -INFINITY) {
+#pragma unroll 4
+      for (int s = 0; s < S; ++s) {
+        const float w = ex2((__ldcg(p.partial_lse + base + s) - Lf) * kLog2e);
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(p.partial_o + (base + s) * DV + d));
+        o0 += w * v.x;
+        o1 += w * v.y;
+      }
+    }
+    const int64_t qrow = u.qo_begin + i;
+    const uint32_t packed =
+        (uint32_t)f32_to_bf16_bits(o0) | ((uint32_t)f32_to_bf16_bits(o1) << 16);
+    *reinterpret_cast<uint32_t*>(p.out + (qrow * Hq + head) * DV + d) = packed;
+    if (d == 0 && p.lse) p.lse[qrow * Hq + head] = Lf;
+  }
+}
+
+}  // namespace nvfp4kv

@@ -16,7 +16,8 @@ constexpr int kBlock = 16;  // elements per E4M3 scale
 // of kv_indices belong to request b; the unit covers its tokens
 // [tok_begin, tok_begin + 16*num_pages) clipped to kv_len.  The partial state
 // of query row i, head h (of the unit's kv head) lives at
-//   partial_base + (i * Hq + h) * num_splits + split      (when split).
+//   partial_base + (i * Hq + h) * num_splits + split      (when split),
+// and `pair` numbers the (request, kv head) for the merge counters.
 struct alignas(16) WorkUnit {
   int32_t b;
   int32_t h_kv;
@@ -29,7 +30,7 @@ struct alignas(16) WorkUnit {
   int32_t split;        // chunk index of this unit within the request
   int32_t num_splits;   // chunks of the request
   int32_t partial_base; // first partial index of request b
-  int32_t pad;
+  int32_t pair;         // index of (b, h_kv) among the split groups
 };
 static_assert(sizeof(WorkUnit) == 48, "WorkUnit layout");
 
@@ -58,6 +59,7 @@ struct AttendParams {
   float* lse;           // [rows, Hq] or null
   float* partial_o;     // [num_partials, Dv]
   float* partial_lse;   // [num_partials]
+  int* counters;        // [pairs * row_blocks] arrival counters (split)
   uint32_t* flags;
 };
 

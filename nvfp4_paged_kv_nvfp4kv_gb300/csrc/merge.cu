@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
     L = M + logf(S);
+#pragma unroll 4
     for (int i = beg; i < end; ++i) {
       const float w = expf(lse_part[i] - L);
       const float* src = o_part + static_cast<int64_t>(i) * dv + lane * PER;

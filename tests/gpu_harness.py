@@ -98,9 +98,20 @@ def bf16_round(x: np.ndarray) -> np.ndarray:
     return torch.from_numpy(x).to(torch.bfloat16).double().numpy()
 
 
+def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
+    """Half a bf16 ulp at |x| (8 significant bits)."""
+    a = np.maximum(np.abs(x), 2.0 ** -126)
+    return 0.5 * 2.0 ** (np.floor(np.log2(a)) - 7)
+
+
 def compare(out_gpu, lse_gpu, out_orc, lse_orc, atol=OUT_ATOL, lse_atol=LSE_ATOL):
-    """Element-wise comparison on the rows the oracle computed.  Returns the
-    error statistics; asserts the tolerances and that nothing is NaN."""
+    """Element-wise comparison on the rows the oracle computed.
+
+    The output is bf16, so even an exact result differs from the float64
+    oracle by up to half a bf16 ulp (0.0078 once |o| >= 2); the 5e-3 budget
+    is applied to the arithmetic on top of that rounding:
+    |gpu - oracle| <= 5e-3 + ulp_bf16(max(|gpu|, |oracle|)) / 2.
+    Returns the error statistics; asserts the tolerances and no NaN."""
     og = out_gpu.float().cpu().double().numpy()
     lg = lse_gpu.cpu().double().numpy()
     sel = ~np.isnan(lse_orc)
@@ -109,16 +120,18 @@ def compare(out_gpu, lse_gpu, out_orc, lse_orc, atol=OUT_ATOL, lse_atol=LSE_ATOL
     assert not np.isnan(lg[sel]).any(), "NaN in GPU lse"
     d = np.abs(og[sel] - out_orc[sel])
     dl = np.abs(lg[sel] - lse_orc[sel])
+    excess = d - bf16_half_ulp(np.maximum(np.abs(og[sel]), np.abs(out_orc[sel])))
     ref = out_orc[sel].reshape(-1)
     got = og[sel].reshape(-1)
     stats = {
         "max_abs": float(d.max()),
+        "max_abs_beyond_bf16_rounding": float(excess.max()),
         "max_abs_vs_bf16_oracle": float(np.abs(og[sel] - bf16_round(out_orc[sel])).max()),
         "lse_max_abs": float(dl.max()),
         "alpha": float(np.dot(got, ref) / np.dot(ref, ref)) if np.dot(ref, ref) > 0 else 1.0,
         "nan": int(np.isnan(og).sum()),
     }
-    assert stats["max_abs"] <= atol, stats
+    assert stats["max_abs_beyond_bf16_rounding"] <= atol, stats
     assert stats["lse_max_abs"] <= lse_atol, stats
     return stats
 

@@ -14,7 +14,7 @@ from nvfp4_paged_kv_nvfp4kv_gb300 import workloads as W
 
 UNIT_DTYPE = np.dtype([(n, "<i4") for n in (
     "b", "h_kv", "page_begin", "num_pages", "tok_begin", "kv_len", "qo_begin", "qo_len",
-    "split", "num_splits", "partial_base", "pad")])
+    "split", "num_splits", "partial_base", "pair")])
 
 
 def test_library_exports_header_symbols():

@@ -72,6 +72,18 @@ def test_split_and_unsplit_agree():
     assert float((l_split - l_un).abs().max()) <= 1e-4
 
 
+def test_standalone_merge_reproduces_fused_merge():
+    batch, g, oc, pt, _ = case("long_context_decode")
+    out, lse = g.run()
+    out2, lse2 = out.clone(), lse.clone()
+    H.N.nvfp4kv_decode_merge(g.plan, out2, lse2)
+    torch.cuda.synchronize()
+    a, b = out.float(), out2.float()
+    ulp = 2.0 ** (torch.floor(torch.log2(torch.clamp(b.abs(), min=2 ** -126))) - 7)
+    assert bool(((a - b).abs() <= ulp).all())
+    assert float((lse - lse2).abs().max()) <= 1e-5
+
+
 @pytest.mark.parametrize("chunk", [16, 32, 48, 1024, 2048])
 def test_forced_chunk_sweep(chunk):
     batch, g, oc, pt, _ = case("long_context_decode")
