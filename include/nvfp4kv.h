@@ -69,6 +69,8 @@ typedef enum nvfp4kv_status {
 /* Bits of the device flag word (see nvfp4kv_workspace_flags). */
 #define NVFP4KV_FLAG_BAD_PAGE_INDEX 0x1u   /* a kv_indices entry out of pool  */
 #define NVFP4KV_FLAG_BAD_APPEND_TARGET 0x2u /* append token outside its request */
+#define NVFP4KV_FLAG_COPY_TIMEOUT 0x4u  /* a page copy did not complete in time;
+                                           the affected rows are not valid   */
 
 const char* nvfp4kv_status_string(int status);
 const char* nvfp4kv_last_error_detail(void);
@@ -88,8 +90,9 @@ typedef struct nvfp4kv_paged_cache {
   int32_t num_kv_heads;
   int32_t head_dim_qk; /* (Dk, Dv) in {(64,64), (128,128), (256,256),        */
   int32_t head_dim_vo; /*  (256,128), (512,256)}; others: UNSUPPORTED         */
-  float k_global_scale; /* dequantised K = e2m1 * E4M3 scale * k_global_scale */
-  float v_global_scale; /* dequantised V uses its own global scale           */
+  float k_global_scale; /* dequantised K = e2m1 * E4M3 scale * k_global_scale;
+                           in [2^-64, 2^64]                                  */
+  float v_global_scale; /* dequantised V uses its own global scale (same range) */
 } nvfp4kv_paged_cache;
 /* Alignment: data pointers and data strides are multiples of 16 bytes; scale
  * pointers and scale strides are multiples of min(16, D/16) bytes. */

@@ -24,6 +24,7 @@ ERR_DEVICE_CHECK = 5
 ERR_PLAN_MISMATCH = 6
 FLAG_BAD_PAGE_INDEX = 0x1
 FLAG_BAD_APPEND_TARGET = 0x2
+FLAG_COPY_TIMEOUT = 0x4
 
 
 class PagedCacheStruct(C.Structure):

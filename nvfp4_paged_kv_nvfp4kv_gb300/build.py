@@ -43,13 +43,14 @@ def _deps():
                                                   os.path.abspath(__file__)]
 
 
-def _compile(src: str, cuda: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _compile(src: str, cuda: str, verbose: bool, build_dir: str = BUILD,
+             defines=()) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
     inc = ["-I", INCLUDE, "-I", CSRC, "-I", os.path.join(cuda, "include")]
     if src.endswith(".cu"):
         cmd = [os.path.join(cuda, "bin", "nvcc"), *ARCH, "-lineinfo", "-O3",
                "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
-               *inc, "-c", src, "-o", obj]
+               *["-D" + d for d in defines], *inc, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
     else:
@@ -63,25 +64,31 @@ def _compile(src: str, cuda: str, verbose: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link the library if any source is newer than it."""
-    if not force and os.path.exists(LIB):
-        t = os.path.getmtime(LIB)
+def build(force: bool = False, verbose: bool = False, defines=(), out: str = None) -> str:
+    """Compile and link the library if any source is newer than it.
+
+    ``defines`` adds -D flags to the CUDA sources (the kernels' launch-shape
+    defaults can be overridden that way) and ``out`` builds into another
+    path instead of the package's own library."""
+    lib = out or LIB
+    build_dir = os.path.dirname(lib)
+    if not force and os.path.exists(lib):
+        t = os.path.getmtime(lib)
         if all(os.path.getmtime(d) <= t for d in _deps()):
-            return LIB
+            return lib
     cuda = _cuda_home()
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, cuda, verbose), srcs))
-    tmp = LIB + ".tmp%d" % os.getpid()
+        objs = list(ex.map(lambda s: _compile(s, cuda, verbose, build_dir, defines), srcs))
+    tmp = lib + ".tmp%d" % os.getpid()
     cmd = [os.path.join(cuda, "bin", "nvcc"), *ARCH, "-shared", "-o", tmp, *objs,
            "-cudart=static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed: %s\n%s%s" % (" ".join(cmd), r.stdout, r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -15,7 +15,7 @@
 #include "internal.h"
 
 namespace nvfp4kv {
-bool attend_config_tc(int dk, int dv, int rows, AttendConfig* cfg);
+bool attend_config_tc(int dk, int dv, int rows, bool bulk, AttendConfig* cfg);
 bool attend_config_simt(int dk, int dv, int rows, AttendConfig* cfg);
 cudaError_t prepare_kernel(const AttendConfig& cfg);
 }  // namespace nvfp4kv
@@ -78,9 +78,10 @@ int check_cache(const nvfp4kv_paged_cache* c, bool for_attention) {
                 "attention head dims (%d, %d) not built; supported: (64,64), "
                 "(128,128), (256,256), (256,128), (512,256)",
                 c->head_dim_qk, c->head_dim_vo);
-  if (!(c->k_global_scale > 0.f) || !std::isfinite(c->k_global_scale) ||
-      !(c->v_global_scale > 0.f) || !std::isfinite(c->v_global_scale))
-    return fail(NVFP4KV_ERR_INVALID_ARGUMENT, "global scales must be finite and > 0");
+  const float gmin = std::ldexp(1.0f, -64), gmax = std::ldexp(1.0f, 64);
+  if (!(c->k_global_scale >= gmin && c->k_global_scale <= gmax) ||
+      !(c->v_global_scale >= gmin && c->v_global_scale <= gmax))
+    return fail(NVFP4KV_ERR_INVALID_ARGUMENT, "global scales must lie in [2^-64, 2^64]");
   const int64_t kd[3] = {c->k_stride_page, c->k_stride_slot, c->k_stride_head};
   const int64_t vd[3] = {c->v_stride_page, c->v_stride_slot, c->v_stride_head};
   const int64_t ks[3] = {c->k_sf_stride_page, c->k_sf_stride_slot, c->k_sf_stride_head};
@@ -122,10 +123,25 @@ CacheView view_of(const nvfp4kv_paged_cache* c) {
   return v;
 }
 
-bool lookup_kernel(int kind, int dk, int dv, int rows, AttendConfig* cfg) {
-  if (kind == kKernelTensorCore) return attend_config_tc(dk, dv, rows, cfg);
+bool lookup_kernel(int kind, int dk, int dv, int rows, bool bulk, AttendConfig* cfg) {
+  if (kind == kKernelTensorCore) return attend_config_tc(dk, dv, rows, bulk, cfg);
   if (kind == kKernelCudaCore) return attend_config_simt(dk, dv, rows, cfg);
   return false;
+}
+
+// The rows of one (page, head) are contiguous in all four buffers and every
+// (page, head) block starts 16-byte aligned: pages can move by bulk copies.
+bool bulk_eligible(const nvfp4kv_paged_cache* c) {
+  auto ok = [](const void* base, int64_t sp, int64_t ss, int64_t sh, int64_t row) {
+    return ss == row && sp % 16 == 0 && sh % 16 == 0 && (16 * row) % 16 == 0 &&
+           reinterpret_cast<uintptr_t>(base) % 16 == 0;
+  };
+  return ok(c->k_data, c->k_stride_page, c->k_stride_slot, c->k_stride_head, c->head_dim_qk / 2) &&
+         ok(c->v_data, c->v_stride_page, c->v_stride_slot, c->v_stride_head, c->head_dim_vo / 2) &&
+         ok(c->k_sf, c->k_sf_stride_page, c->k_sf_stride_slot, c->k_sf_stride_head,
+            c->head_dim_qk / 16) &&
+         ok(c->v_sf, c->v_sf_stride_page, c->v_sf_stride_slot, c->v_sf_stride_head,
+            c->head_dim_vo / 16);
 }
 
 constexpr int kMinChunkPages = 8;
@@ -272,7 +288,8 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
   int kind = opts.kernel;
   AttendConfig cfg{};
   if (kind == 0) kind = kKernelTensorCore;
-  if (!lookup_kernel(kind, head_dim_qk, head_dim_vo, max_rows <= 8 ? 8 : 16, &cfg))
+  // occupancy is sized on the bulk-copy variant (the contiguous-page path)
+  if (!lookup_kernel(kind, head_dim_qk, head_dim_vo, max_rows <= 8 ? 8 : 16, true, &cfg))
     return fail(NVFP4KV_ERR_UNSUPPORTED, "no %s kernel for head dims (%d, %d)",
                 kind == kKernelTensorCore ? "tensor-core" : "CUDA-core", head_dim_qk,
                 head_dim_vo);
@@ -503,7 +520,7 @@ int nvfp4kv_decode_attend(const nvfp4kv_plan_info* info, const void* q_bf16,
   if (info->num_units == 0) return ok();
   AttendConfig cfg{};
   if (!lookup_kernel(info->kernel, info->head_dim_qk, info->head_dim_vo, info->rows_per_block,
-                     &cfg))
+                     bulk_eligible(cache), &cfg))
     return fail(NVFP4KV_ERR_UNSUPPORTED, "planned kernel not available");
   cudaError_t e = prepare_kernel(cfg);
   if (e != cudaSuccess) return cuda_fail(e, "kernel attributes");

@@ -59,7 +59,6 @@ __global__ void __launch_bounds__(WARPS * 32) attend_simt_kernel(const AttendPar
   const int row0 = blockIdx.y * RB;
   if (row0 >= R) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int Hq = p.num_qo_heads;
 
   for (int idx = tid; idx < RB * DK; idx += WARPS * 32) {
     const int rr = idx / DK, d = idx % DK, r = row0 + rr;

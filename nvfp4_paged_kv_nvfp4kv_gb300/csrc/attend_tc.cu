@@ -34,6 +34,7 @@
 //    for the merge when the plan split the request.
 #include <cfloat>
 #include <cstdint>
+#include <type_traits>
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -48,9 +49,15 @@ namespace {
 
 using namespace dev;
 
-template <int DK, int DV, int NT, int WARPS, int STAGES>
-struct TcTraits : PageStage<DK, DV> {
-  using S = PageStage<DK, DV>;
+// Q fragments of the small shapes live in registers (1) or are re-read from
+// shared memory at every k-step (0).
+#ifndef NVFP4KV_TC_QREGS
+#define NVFP4KV_TC_QREGS 1
+#endif
+
+template <int DK, int DV, int NT, int WARPS, int STAGES, bool BULK>
+struct TcTraits : PageStage<DK, DV, BULK> {
+  using S = PageStage<DK, DV, BULK>;
   static constexpr int RB = 8 * NT;                  // query rows per CTA
   static constexpr int CB = (DK / 8 < 16) ? DK / 8 : 16;  // K bytes per lane chunk
   static constexpr int NCH = (DK / 8) / CB;          // K chunks per lane
@@ -63,15 +70,29 @@ struct TcTraits : PageStage<DK, DV> {
   static constexpr int MAIN_BYTES = PIPE_BYTES > COMB_BYTES ? PIPE_BYTES : COMB_BYTES;
   static constexpr int QROW = DK + 8;                // f16 elements, padded
   static constexpr int Q_BYTES = RB * QROW * 2;
-  static constexpr int SMEM = MAIN_BYTES + Q_BYTES + RB * 16;
-  static constexpr bool Q_IN_REGS = KSTEPS * 2 * NT <= 32;
+  static constexpr int BAR_BYTES = WARPS * STAGES * 8;  // one mbarrier per stage
+  static constexpr int SMEM = MAIN_BYTES + Q_BYTES + RB * 16 + BAR_BYTES;
+  static constexpr bool Q_IN_REGS = NVFP4KV_TC_QREGS && KSTEPS * 2 * NT <= 32;
   static_assert(S::VC == VC, "V lane chunk");
 };
 
-template <int DK, int DV, int NT, int WARPS, int STAGES>
-__global__ void __launch_bounds__(WARPS * 32)
+// Resident CTAs per SM asked of the register allocator for the small decode
+// shapes (D <= 128, 8 rows); the larger shapes keep what they need.
+#ifndef NVFP4KV_TC_MINB
+#define NVFP4KV_TC_MINB 4
+#endif
+template <int DK, int DV, int NT>
+constexpr int tc_min_blocks() {
+  return (DK <= 128 && DV <= 128 && NT == 1) ? NVFP4KV_TC_MINB : 1;
+}
+
+// Polls of a stage's barrier before the kernel gives up on a bulk copy.
+constexpr uint32_t kWaitLimit = 1u << 20;
+
+template <int DK, int DV, int NT, int WARPS, int STAGES, bool BULK>
+__global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
     attend_tc_kernel(const AttendParams p) {
-  using T = TcTraits<DK, DV, NT, WARPS, STAGES>;
+  using T = TcTraits<DK, DV, NT, WARPS, STAGES, BULK>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* pipe = smem;
   uint16_t* sQ = reinterpret_cast<uint16_t*>(smem + T::MAIN_BYTES);
@@ -85,39 +106,118 @@ __global__ void __launch_bounds__(WARPS * 32)
   if (row0 >= R) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
-  const int Hq = p.num_qo_heads;
 
-  // ---- Q: load, per-row power-of-two prescale into f16, row limits -------
-  for (int rr = warp; rr < T::RB; rr += WARPS) {
-    const int r = row0 + rr;
-    uint16_t* dst = sQ + rr * T::QROW;
-    if (r >= R) {
-      for (int d = lane; d < DK; d += 32) dst[d] = 0;
-      if (lane == 0) {
-        sRowF[rr] = 0.f;
-        sRowLim[rr] = -1;
-      }
-      continue;
-    }
-    const int i = r / G, gh = r % G;
-    const uint16_t* src = p.q + (int64_t)(u.qo_begin + i) * p.q_stride_tok +
-                          (int64_t)(u.h_kv * G + gh) * p.q_stride_head;
-    float amax = 0.f;
-    for (int d = lane; d < DK; d += 32)
-      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(src[d])));
+  // ---- Q rows of this CTA: one 16-byte load per thread per chunk of 8
+  // elements, issued now and consumed after the pipeline has started ------
+  constexpr int QCH = T::RB * DK / 8;                      // 8-element chunks
+  constexpr int QPT = (QCH + WARPS * 32 - 1) / (WARPS * 32);
+  uint4 qv[QPT];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  for (int k = 0; k < QPT; ++k) {
+    const int ci = tid + k * WARPS * 32;
+    const int rr = ci / (DK / 8), r = row0 + rr;
+    qv[k] = make_uint4(0u, 0u, 0u, 0u);
+    if (ci < QCH && r < R) {
+      const int i = r / G, gh = r % G;
+      qv[k] = *reinterpret_cast<const uint4*>(p.q + (int64_t)(u.qo_begin + i) * p.q_stride_tok +
+                                              (int64_t)(u.h_kv * G + gh) * p.q_stride_head +
+                                              (ci % (DK / 8)) * 8);
+    }
+  }
+  if (tid < T::RB) reinterpret_cast<int*>(sRowF)[tid] = 0;  // per-row amax bits
+
+  // ---- start the page pipeline: the first pages' copies are in flight
+  // while Q is prepared ---------------------------------------------------
+  uint8_t* wpipe = pipe + warp * STAGES * T::STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::MAIN_BYTES + T::Q_BYTES + T::RB * 16) +
+                   warp * STAGES;
+  if constexpr (BULK) {
+    if (lane == 0) {
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+      mbar_init_fence();
+    }
+    __syncwarp();
+  }
+  const int npw = u.num_pages > warp ? (u.num_pages - warp + WARPS - 1) / WARPS : 0;
+  const int32_t* pidx = p.kv_indices + u.page_begin;
+
+  // page ids are read one iteration before their copies are issued, so the
+  // address computation never waits on a global load
+  auto page_id = [&](int i) -> int32_t {
+    return i < npw ? pidx[warp + i * WARPS] : 0;
+  };
+  auto load_page = [&](int i, int32_t pid) {
+    if (pid < 0 || pid >= p.cache.num_pages) {
+      if (lane == 0) atomicOr(p.flags, 0x1u);
+      pid = 0;
+    }
+    if constexpr (BULK) {
+      if (lane == 0)
+        issue_page_bulk<typename T::S>(wpipe + (i % STAGES) * T::STAGE_BYTES,
+                                       &bars[i % STAGES], p.cache, pid, u.h_kv);
+    } else {
+      issue_page<typename T::S>(wpipe + (i % STAGES) * T::STAGE_BYTES, p.cache, pid, u.h_kv,
+                                lane);
+    }
+  };
+
+#pragma unroll
+  for (int s = 0; s < STAGES - 1; ++s) {
+    if (s < npw) load_page(s, page_id(s));
+    if constexpr (!BULK) cp_async_commit();
+  }
+  int32_t next_pid = page_id(STAGES - 1);
+
+  // ---- Q: per-row power-of-two prescale into f16, row limits ------------
+  // amax of each row (non-negative floats order like their bit patterns)
+  __syncthreads();  // the amax slots are zeroed
+#pragma unroll
+  for (int k = 0; k < QPT; ++k) {
+    const int ci = tid + k * WARPS * 32;
+    if (ci >= QCH) continue;
+    const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
+    float am = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      am = fmaxf(am, fmaxf(fabsf(bf16_bits_to_f32(w[j] & 0xFFFFu)),
+                           fabsf(bf16_bits_to_f32(w[j] >> 16))));
+    atomicMax(reinterpret_cast<int*>(sRowF) + ci / (DK / 8), __float_as_int(am));
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < QPT; ++k) {
+    const int ci = tid + k * WARPS * 32;
+    if (ci >= QCH) continue;
+    const int rr = ci / (DK / 8);
+    const float amax = __int_as_float(reinterpret_cast<const int*>(sRowF)[rr]);
     // e such that amax * 2^e lies in [2^14, 2^15)
     int e = 0;
     if (amax > 0.f) e = 14 - (int)((__float_as_uint(amax) >> 23) & 0xFF) + 127;
     e = max(-120, min(120, e));
     const float up = __uint_as_float((uint32_t)(127 + e) << 23);
-    for (int d = lane; d < DK; d += 32)
-      dst[d] = __half_as_ushort(__float2half_rn(bf16_bits_to_f32(src[d]) * up));
-    if (lane == 0) {
-      sRowF[rr] = p.qk_scale_log2 * __uint_as_float((uint32_t)(127 - e) << 23);
-      sRowLim[rr] = p.causal ? (u.kv_len - u.qo_len + i) : (u.kv_len - 1);
+    const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
+    uint32_t h[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      h[j] = f32x2_to_f16x2(bf16_bits_to_f32(w[j] & 0xFFFFu) * up,
+                            bf16_bits_to_f32(w[j] >> 16) * up);
+    *reinterpret_cast<uint4*>(sQ + rr * T::QROW + (ci % (DK / 8)) * 8) =
+        make_uint4(h[0], h[1], h[2], h[3]);
+    if (ci % (DK / 8) == 0) {
+      const int r = row0 + rr;
+      sRowLim[rr] = r >= R ? -1 : (p.causal ? (u.kv_len - u.qo_len + r / G) : (u.kv_len - 1));
+      // the row factor replaces the amax slot once every thread has read it
+      qv[k].x = __float_as_uint(r >= R ? 0.f
+                                       : p.qk_scale_log2 *
+                                             __uint_as_float((uint32_t)(127 - e) << 23));
     }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < QPT; ++k) {
+    const int ci = tid + k * WARPS * 32;
+    if (ci < QCH && ci % (DK / 8) == 0) sRowF[ci / (DK / 8)] = __uint_as_float(qv[k].x);
   }
   __syncthreads();
 
@@ -171,40 +271,40 @@ __global__ void __launch_bounds__(WARPS * 32)
 #pragma unroll
       for (int k = 0; k < 4; ++k) oacc[mt][nq][k] = 0.f;
 
-  uint8_t* wpipe = pipe + warp * STAGES * T::STAGE_BYTES;
-  const int npw = u.num_pages > warp ? (u.num_pages - warp + WARPS - 1) / WARPS : 0;
-  const int32_t* pidx = p.kv_indices + u.page_begin;
-
-  auto load_page = [&](int i) {
-    int32_t pid = pidx[warp + i * WARPS];
-    if (pid < 0 || pid >= p.cache.num_pages) {
-      if (lane == 0) atomicOr(p.flags, 0x1u);
-      pid = 0;
-    }
-    issue_page<typename T::S>(wpipe + (i % STAGES) * T::STAGE_BYTES, p.cache, pid, u.h_kv,
-                              lane);
-  };
-
-#pragma unroll
-  for (int s = 0; s < STAGES - 1; ++s) {
-    if (s < npw) load_page(s);
-    cp_async_commit();
-  }
 
   for (int i = 0; i < npw; ++i) {
-    if (i + STAGES - 1 < npw) load_page(i + STAGES - 1);
-    cp_async_commit();
-    cp_async_wait<STAGES - 1>();
+    if (i + STAGES - 1 < npw) load_page(i + STAGES - 1, next_pid);
+    next_pid = page_id(i + STAGES);
+    if constexpr (BULK) {
+      const bool ok = mbar_wait_bounded(&bars[i % STAGES], (i / STAGES) & 1, kWaitLimit);
+      if (!__all_sync(0xffffffffu, ok)) {
+        // a copy did not land: flag it, wait (bounded) for the copies this
+        // warp still has in flight, and finish without the remaining pages
+        if (lane == 0) atomicOr(p.flags, 0x4u);
+        const int last = min(npw, i + STAGES) - 1;
+        for (int j = i + 1; j <= last; ++j)
+          mbar_wait_bounded(&bars[j % STAGES], (j / STAGES) & 1, kWaitLimit);
+        break;
+      }
+    } else {
+      cp_async_commit();
+      cp_async_wait<STAGES - 1>();
+    }
     __syncwarp();
     const uint8_t* st = wpipe + (i % STAGES) * T::STAGE_BYTES;
     const int tok0 = u.tok_begin + (warp + i * WARPS) * 16;
 
     // ---- S = Q K^T for tokens tok0 .. tok0+15 (two n-tiles) -------------
-    float sacc[2][4];
+    // two accumulators per n-tile (alternate k-steps) halve the dependent
+    // mma chain; they are added after the last k-step
+    float sacc[2][4], sacc2[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int k = 0; k < 4; ++k) sacc[nt][k] = 0.f;
+      for (int k = 0; k < 4; ++k) {
+        sacc[nt][k] = 0.f;
+        sacc2[nt][k] = 0.f;
+      }
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const int row = 8 * nt + g;
@@ -249,10 +349,14 @@ __global__ void __launch_bounds__(WARPS * 32)
             q_frag(kk + 1, a1);
           }
           mma_16816(sacc[nt], a0, h[0], h[1]);
-          mma_16816(sacc[nt], a1, h[2], h[3]);
+          mma_16816(sacc2[nt], a1, h[2], h[3]);
         }
       }
     }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sacc[nt][k] += sacc2[nt][k];
 
     // ---- online softmax (log2 domain), rows g and g+8 -------------------
     const bool need_mask = tok0 + 15 > min_lim;
@@ -344,29 +448,44 @@ __global__ void __launch_bounds__(WARPS * 32)
         sA[bl] = e4m3x2_to_f16x2(s0 | (s1 << 8));
         sB[bl] = e4m3x2_to_f16x2(s2 | (s3 << 8));
       }
+      // Interleave the nibbles of two tokens' bytes before converting: for
+      // words W0 (token 2t) and W1 (token 2t+1), X holds in each byte the
+      // even-dim code of W0 (low nibble) and of W1 (high nibble), Y the
+      // odd-dim codes, so cvt(X byte j) = {v[2t][d], v[2t+1][d]} is A row g
+      // and cvt(Y byte j) is A row g+8 of m-tile 4wq+j.
+      constexpr uint32_t kLoNib = 0x0F0F0F0Fu;
 #pragma unroll
       for (int wq = 0; wq < VW; ++wq) {
-        uint32_t h[4][4];
+        uint32_t x[2], y[2];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) e2m1x8_to_f16x8(vw[k][wq], h[k]);
-#pragma unroll
-        for (int j = 0; j < 4 && 4 * wq + j < T::VC; ++j) {
+        for (int pr = 0; pr < 2; ++pr) {
+          const uint32_t w0 = vw[2 * pr][wq], w1 = vw[2 * pr + 1][wq];
+          x[pr] = (w0 & kLoNib) | ((w1 << 4) & ~kLoNib);
+          y[pr] = ((w0 >> 4) & kLoNib) | (w1 & ~kLoNib);
+        }
+        auto mtile = [&](auto jc) {
+          constexpr int j = decltype(jc)::value;
           const int mt = 4 * wq + j;
+          if (mt >= T::VC) return;
           const int bl = (mt * 2) / 16;
           uint32_t a[4];
-          a[0] = hmul2(pack_lo(h[0][j], h[1][j]), sA[bl]);
-          a[1] = hmul2(pack_hi(h[0][j], h[1][j]), sA[bl]);
-          a[2] = hmul2(pack_lo(h[2][j], h[3][j]), sB[bl]);
-          a[3] = hmul2(pack_hi(h[2][j], h[3][j]), sB[bl]);
+          a[0] = hmul2(e2m1x2_byte_to_f16x2<j>(x[0]), sA[bl]);
+          a[1] = hmul2(e2m1x2_byte_to_f16x2<j>(y[0]), sA[bl]);
+          a[2] = hmul2(e2m1x2_byte_to_f16x2<j>(x[1]), sB[bl]);
+          a[3] = hmul2(e2m1x2_byte_to_f16x2<j>(y[1]), sB[bl]);
 #pragma unroll
           for (int nq = 0; nq < NT; ++nq)
             mma_16816(oacc[mt][nq], a, pfrag[nq][0], pfrag[nq][1]);
-        }
+        };
+        mtile(std::integral_constant<int, 0>{});
+        mtile(std::integral_constant<int, 1>{});
+        mtile(std::integral_constant<int, 2>{});
+        mtile(std::integral_constant<int, 3>{});
       }
     }
     __syncwarp();
   }
-  cp_async_wait<0>();
+  if constexpr (!BULK) cp_async_wait<0>();
 
   // ---- combine the warps ------------------------------------------------
 #pragma unroll
@@ -401,27 +520,40 @@ __global__ void __launch_bounds__(WARPS * 32)
   finish_unit<T::RB, DV, WARPS>(p, u, row0, R, sM, sL, sO, sRowF);
 }
 
-template <int DK, int DV, int NT>
+// Launch shape (compile-time; the defaults are the tuned values).
+#ifndef NVFP4KV_TC_WARPS
+#define NVFP4KV_TC_WARPS 4
+#endif
+#ifndef NVFP4KV_TC_STAGES
+#define NVFP4KV_TC_STAGES 4
+#endif
+
+template <int DK, int DV, int NT, bool BULK>
 bool make_tc(AttendConfig* cfg) {
-  constexpr int WARPS = 4, STAGES = DK >= 512 ? 3 : 4;
-  using T = TcTraits<DK, DV, NT, WARPS, STAGES>;
+  constexpr int WARPS = NVFP4KV_TC_WARPS;
+  constexpr int STAGES = DK >= 512 ? 3 : NVFP4KV_TC_STAGES;
+  using T = TcTraits<DK, DV, NT, WARPS, STAGES, BULK>;
   cfg->kind = kKernelTensorCore;
   cfg->dk = DK;
   cfg->dv = DV;
   cfg->rows = T::RB;
   cfg->warps = WARPS;
   cfg->smem_bytes = T::SMEM;
-  cfg->func = reinterpret_cast<const void*>(attend_tc_kernel<DK, DV, NT, WARPS, STAGES>);
+  cfg->func =
+      reinterpret_cast<const void*>(attend_tc_kernel<DK, DV, NT, WARPS, STAGES, BULK>);
   return true;
 }
 
 }  // namespace
 
-bool attend_config_tc(int dk, int dv, int rows, AttendConfig* cfg) {
+bool attend_config_tc(int dk, int dv, int rows, bool bulk, AttendConfig* cfg) {
   const int nt = rows <= 8 ? 1 : 2;
-#define NVFP4KV_TC_CASE(DK_, DV_)                                      \
-  if (dk == DK_ && dv == DV_) return nt == 1 ? make_tc<DK_, DV_, 1>(cfg) \
-                                             : make_tc<DK_, DV_, 2>(cfg);
+#define NVFP4KV_TC_CASE(DK_, DV_)                                             \
+  if (dk == DK_ && dv == DV_) {                                               \
+    if (bulk) return nt == 1 ? make_tc<DK_, DV_, 1, true>(cfg)                \
+                             : make_tc<DK_, DV_, 2, true>(cfg);               \
+    return nt == 1 ? make_tc<DK_, DV_, 1, false>(cfg) : make_tc<DK_, DV_, 2, false>(cfg); \
+  }
   NVFP4KV_TC_CASE(64, 64)
   NVFP4KV_TC_CASE(128, 128)
   NVFP4KV_TC_CASE(256, 256)

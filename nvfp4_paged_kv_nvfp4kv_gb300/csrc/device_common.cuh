@@ -37,6 +37,48 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
+// ---- mbarrier + bulk copy (cp.async.bulk, completion counted in bytes) ----
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_addr(bar)), "r"(count));
+}
+// make the initialised barriers visible to the bulk-copy (async) proxy
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase with the given parity to complete, giving up after
+// `limit` polls (each poll may suspend the thread for a short while).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint32_t limit) {
+  for (uint32_t it = 0; it < limit; ++it)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// global -> shared bulk copy; `bytes` and both addresses are multiples of 16
+__device__ __forceinline__ void bulk_g2s(void* smem, const void* gmem, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];\n" ::"r"(smem_addr(smem)),
+      "l"(gmem), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
 // Four packed bytes (8 e2m1 codes) -> four f16x2: h[j] holds byte j, its low
 // nibble (the even element) in the low half.
 __device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t (&h)[4]) {
@@ -50,6 +92,27 @@ __device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t (&h)[4]) {
       "}\n"
       : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
       : "r"(w));
+}
+
+// Byte J of w (2 e2m1 codes) -> f16x2, its low nibble in the low half.
+template <int J>
+__device__ __forceinline__ uint32_t e2m1x2_byte_to_f16x2(uint32_t w) {
+  static_assert(J >= 0 && J < 4, "byte index");
+  uint32_t h;
+  if constexpr (J == 0) {
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n}\n" : "=r"(h) : "r"(w));
+  } else if constexpr (J == 1) {
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b1;\n}\n" : "=r"(h) : "r"(w));
+  } else if constexpr (J == 2) {
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b2;\n}\n" : "=r"(h) : "r"(w));
+  } else {
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b3;\n}\n" : "=r"(h) : "r"(w));
+  }
+  return h;
 }
 
 // Two E4M3 bytes (low byte -> low half) -> f16x2.  Every E4M3 value is exact

@@ -114,12 +114,23 @@ __device__ __forceinline__ void finish_unit(const AttendParams& p, const WorkUni
     const float Lf = sFin[rr];
     float o0 = 0.f, o1 = 0.f;
     if (Lf != -INFINITY) {
-#pragma unroll 4
-      for (int s = 0; s < S; ++s) {
-        const float w = ex2((__ldcg(p.partial_lse + base + s) - Lf) * kLog2e);
-        const float2 v = __ldcg(reinterpret_cast<const float2*>(p.partial_o + (base + s) * DV + d));
-        o0 += w * v.x;
-        o1 += w * v.y;
+      // batches of 16 partials: all loads of a batch are in flight together
+      for (int s0 = 0; s0 < S; s0 += 16) {
+        float lw[16];
+        float2 v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (s0 + j < S) {
+            lw[j] = __ldcg(p.partial_lse + base + s0 + j);
+            v[j] = __ldcg(reinterpret_cast<const float2*>(p.partial_o + (base + s0 + j) * DV + d));
+          }
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (s0 + j < S) {
+            const float w = ex2((lw[j] - Lf) * kLog2e);
+            o0 += w * v[j].x;
+            o1 += w * v[j].y;
+          }
       }
     }
     const int64_t qrow = u.qo_begin + i;

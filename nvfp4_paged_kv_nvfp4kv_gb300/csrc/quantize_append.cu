@@ -6,17 +6,22 @@
 //   s = E4M3_RNE_satfinite(amax / (6 g)),
 //   code_i = e2m1_RNE_satfinite(x_i / (s g)) with ties to the even code and
 //   the sign of x_i kept on zero codes, packed low nibble = even element.
-// Every rounding decision is the exact-real one:
-//  * amax / (6 g) is formed in float64 (6g exact; one rounding, which cannot
-//    cross or land on an E4M3 midpoint since the numerator has 8 significant
-//    bits) and rounded to E4M3 by an integer rint on its binade;
-//  * instead of dividing x by s g, |x| is compared with the seven e2m1
-//    midpoints times s g.  Each threshold T = mid * s * g is exact in
-//    float64; it is rounded DOWN to float32 (Tf) with a flag saying whether
-//    that was exact, so |x| > T  <=>  |x| > Tf and |x| == T  <=>  (exact and
-//    |x| == Tf), all in float32 compares.  A tie takes the even code.
-// One thread per block; a token whose request, position or page id is out of
-// range is skipped and flagged.
+// Every rounding decision is the exact-real one, in float32 only (float64 is
+// a slow pipe on this part):
+//  * an approximate t = amax / g / 6 (two correctly rounded divisions, a few
+//    ulps from the exact ratio) is rounded to E4M3 by the hardware RN
+//    conversion; the E4M3 grid is 2^-4 relative or coarser, so the exact
+//    answer is that code or a neighbour, decided by comparing amax with
+//    6 * midpoint * g exactly;
+//  * element codes compare |x| with the seven e2m1 midpoints times s g.
+// An exact comparison of a with m * g (m, g, a positive floats): m * g = P + E
+// exactly with P = RN(m g) and E = fma(m, g, -P); a - P is exact when a and P
+// are within a factor of two and otherwise much larger than |E|, so the sign
+// of (a - P) - E is the sign of a - m g, and zero means a tie.
+// One thread per block; the bf16 loads are issued before the page lookup; a
+// token whose request, position or page id is out of range is skipped and
+// flagged.  Global scales lie in [2^-64, 2^64] (checked on the host), so no
+// product underflows or overflows.
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -27,33 +32,45 @@
 namespace nvfp4kv {
 namespace {
 
-// E4M3 (bias 7, 3 mantissa bits, subnormal spacing 2^-9, max 448) code of a
-// positive finite double, round to nearest even, saturating.
-__device__ __forceinline__ uint32_t e4m3_code_rne_sat(double v) {
-  if (!(v > 0.0)) return 0u;
-  if (v > 448.0) return 0x7Eu;
-  if (v < 0.015625) {                    // below 2^-6: grid m * 2^-9
-    return static_cast<uint32_t>(rint(v * 512.0));  // 8 is the code of 2^-6
-  }
-  const long long bits = __double_as_longlong(v);
-  const int e = static_cast<int>((bits >> 52) & 0x7FF) - 1023;  // v in [2^e, 2^e+1)
-  const double up = __longlong_as_double(static_cast<long long>(1023 + 3 - e) << 52);
-  const uint32_t r = static_cast<uint32_t>(rint(v * up));      // 8 .. 16
-  const uint32_t code = (static_cast<uint32_t>(e + 7) << 3) + (r - 8u);  // 16 carries
-  return code > 0x7Eu ? 0x7Eu : code;
-}
-
 __device__ __forceinline__ float e4m3_code_value(uint32_t code) {
   const uint32_t e = (code >> 3) & 0xF, m = code & 7;
   if (e == 0) return static_cast<float>(m) * (1.0f / 512.0f);
   return __uint_as_float(((e - 7 + 127) << 23) | (m << 20));
 }
 
+// sign(a - m * g), exactly (see the file comment)
+__device__ __forceinline__ int cmp_prod(float a, float m, float g) {
+  const float P = __fmul_rn(m, g);
+  const float E = fmaf(m, g, -P);
+  const float d = __fsub_rn(a, P);
+  return (d > E) - (d < E);
+}
+
+// E4M3 code of amax / (6 g): round to nearest even, saturating at 448.
+__device__ __forceinline__ uint32_t scale_code(float amax, float g) {
+  if (amax == 0.f) return 0u;
+  const float t = __fdiv_rn(__fdiv_rn(amax, g), 6.0f);
+  unsigned short pair;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(pair) : "f"(0.0f), "f"(t));
+  uint32_t c = pair & 0xFFu;
+  if (c > 0u) {  // below the midpoint with the code under c?
+    const float mid = 0.5f * (e4m3_code_value(c - 1) + e4m3_code_value(c));
+    const int sgn = cmp_prod(amax, 6.0f * mid, g);
+    if (sgn < 0 || (sgn == 0 && (c & 1u))) return c - 1;
+  }
+  if (c < 0x7Eu) {  // above the midpoint with the code over c?
+    const float mid = 0.5f * (e4m3_code_value(c) + e4m3_code_value(c + 1));
+    const int sgn = cmp_prod(amax, 6.0f * mid, g);
+    if (sgn > 0 || (sgn == 0 && (c & 1u))) return c + 1;
+  }
+  return c;
+}
+
 __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
   const int bpk = p.head_dim_qk / 16, bpv = p.head_dim_vo / 16;
   const int per = bpk + bpv;
   const int64_t total = static_cast<int64_t>(p.nnz) * p.num_kv_heads * per;
-  const double mids[7] = {0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0};
+  const float mids[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.0f};
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
        idx < total; idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int blk = static_cast<int>(idx % per);
@@ -62,6 +79,13 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
     const int t = static_cast<int>(th / p.num_kv_heads);
     const bool isv = blk >= bpk;
     const int jb = isv ? blk - bpk : blk;
+
+    // the block's bf16 values (independent of the page lookup below)
+    const uint16_t* src = isv ? p.v + t * p.v_stride_tok + h * p.v_stride_head
+                              : p.k + t * p.k_stride_tok + h * p.k_stride_head;
+    src += 16 * jb;
+    const uint4 lo = *reinterpret_cast<const uint4*>(src);
+    const uint4 hi = *reinterpret_cast<const uint4*>(src + 8);
 
     // locate the token's page
     const int b = p.batch_idx[t];
@@ -84,11 +108,6 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
     }
     const int slot = pos % kPageSize;
 
-    const uint16_t* src = isv ? p.v + t * p.v_stride_tok + h * p.v_stride_head
-                              : p.k + t * p.k_stride_tok + h * p.k_stride_head;
-    src += 16 * jb;
-    const uint4 lo = *reinterpret_cast<const uint4*>(src);
-    const uint4 hi = *reinterpret_cast<const uint4*>(src + 8);
     const uint32_t wv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
     float x[16];
 #pragma unroll
@@ -100,18 +119,21 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
 #pragma unroll
     for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(x[k]));
 
-    const double g = isv ? static_cast<double>(p.v_global_scale)
-                         : static_cast<double>(p.k_global_scale);
-    const uint32_t sfb = e4m3_code_rne_sat(static_cast<double>(amax) / (6.0 * g));
+    const float g = isv ? p.v_global_scale : p.k_global_scale;
+    const uint32_t sfb = scale_code(amax, g);
     const float s = e4m3_code_value(sfb);
-    const double sg = static_cast<double>(s) * g;  // exact
+    // thresholds T_k = mid_k * s * g: Tf_k = T_k rounded down to float32 and
+    // whether that was exact.  |x| > T_k <=> |x| > Tf_k for a float |x|; a
+    // tie needs T_k exact (|x| == Tf_k < T_k is simply below the threshold)
     float tf[7];
     bool ex[7];
 #pragma unroll
     for (int k = 0; k < 7; ++k) {
-      const double T = mids[k] * sg;  // exact
-      tf[k] = __double2float_rd(T);
-      ex[k] = static_cast<double>(tf[k]) == T;
+      const float ms = mids[k] * s;  // exact: at most 7 significant bits
+      const float P = __fmul_rn(ms, g);
+      const float E = fmaf(ms, g, -P);
+      tf[k] = E < 0.f ? __uint_as_float(__float_as_uint(P) - 1u) : P;
+      ex[k] = E == 0.f;
     }
     uint32_t packed[2] = {0u, 0u};
 #pragma unroll

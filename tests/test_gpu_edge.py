@@ -25,9 +25,9 @@ def small(**kw):
     return W.make_batch(W.custom_workload(**args))
 
 
-def check(batch, layout="HND", **plan_kw):
-    g = H.GpuCase(batch, layout=layout, **plan_kw)
-    oc, pt = H.oracle_cache(batch, layout)
+def check(batch, layout="HND", pad_page_bytes=0, **plan_kw):
+    g = H.GpuCase(batch, layout=layout, pad_page_bytes=pad_page_bytes, **plan_kw)
+    oc, pt = H.oracle_cache(batch, layout, pad_page_bytes=pad_page_bytes)
     H.compare_cache_bytes(g.cache, oc)
     out, lse = g.run()
     ro, rl = H.oracle_attention(batch, oc, pt)
