@@ -252,6 +252,34 @@ int nvfp4kv_merge_states(const float* o_partial, const float* lse_partial,
                          int32_t head_dim_vo, void* out_bf16, float* lse,
                          cudaStream_t stream);
 
+/* ---- allocation-free variant -------------------------------------------- */
+/* nvfp4kv_decode_run for callers that cannot allocate device memory where
+ * they run attention (device memory fully reserved up front, for example by a
+ * KV-cache pool sized to the GPU; a host framework that provides no scratch
+ * buffer; a path that must not call cudaMalloc because it synchronises the
+ * device).  The pages have no counterpart of it: it exists for deployment.
+ * The workspace is a fixed 16 MiB array inside the library, held by every GPU
+ * that loads the library until the process exits; the call allocates
+ * nothing.  The caller still passes the inputs and the outputs.
+ *   info, plan_host [host]  a plan made by nvfp4kv_decode_plan with
+ *           workspace = NULL (sizes only); info->workspace_bytes must not
+ *           exceed 16 MiB (otherwise WORKSPACE_TOO_SMALL and nothing is
+ *           enqueued).  plan_host is the source of an asynchronous copy: keep
+ *           it unchanged until the work on `stream` has completed.
+ *   the other arguments are those of nvfp4kv_decode_run.
+ * Each call clears the array's flag word and merge counters and copies the
+ * plan's work list into it before the attention kernel, all on `stream`.
+ * The first call on a device looks up the array's device address (with
+ * that device current); make it before any stream capture.  All calls share
+ * the one array: calls whose work overlaps on the GPU (different streams,
+ * or different plans in flight at once) race and must be serialised by the
+ * caller. */
+int nvfp4kv_decode_run_static(const nvfp4kv_plan_info* info, const void* plan_host,
+                              const void* q_bf16, int64_t q_stride_tok,
+                              int64_t q_stride_head, const nvfp4kv_paged_cache* cache,
+                              const int32_t* kv_indices, float sm_scale,
+                              void* out_bf16, float* lse, cudaStream_t stream);
+
 /* ---- flags ---------------------------------------------------------------- */
 /* Read (and optionally clear) the device flag word of a planned workspace.
  * Synchronises `stream`.  Returns NVFP4KV_ERR_DEVICE_CHECK when a flag is set

@@ -17,7 +17,8 @@ from ._lib import NvFp4KvError, PagedCacheStruct, PlanInfo, PlanOptions, check
 
 __all__ = ["PagedCache", "Plan", "NvFp4KvError", "nvfp4kv_quantize_append",
            "nvfp4kv_decode_plan", "nvfp4kv_decode_run", "nvfp4kv_decode_attend",
-           "nvfp4kv_decode_merge", "nvfp4kv_merge_states", "nvfp4kv_workspace_flags"]
+           "nvfp4kv_decode_merge", "nvfp4kv_merge_states", "nvfp4kv_workspace_flags",
+           "nvfp4kv_decode_run_static"]
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -234,6 +235,22 @@ def nvfp4kv_workspace_flags(plan: Plan, clear: bool = False, stream=None) -> int
     if st not in (_lib.OK, _lib.ERR_DEVICE_CHECK):
         check(st, "nvfp4kv_workspace_flags")
     return int(flags.value)
+
+
+def nvfp4kv_decode_run_static(plan: Plan, q: torch.Tensor, cache: PagedCache, kv_indices,
+                              sm_scale: float = 0.0, out=None, lse=None, stream=None):
+    """nvfp4kv_decode_run without a caller workspace: the library's fixed
+    16 MiB array serves as the workspace (for callers that cannot allocate
+    device memory).  ``plan`` is a host-only plan
+    (``nvfp4kv_decode_plan(..., allocate=False)``); ``out``/``lse`` should be
+    passed by such callers (allocated here only when omitted)."""
+    out, lse = _outputs(plan, out, lse, q.device)
+    s = cache.struct()
+    st = _lib.load().nvfp4kv_decode_run_static(
+        C.byref(plan.info), _ptr(plan.host), _ptr(q), q.stride(0), q.stride(1), C.byref(s),
+        _ptr(kv_indices), float(sm_scale or 0.0), _ptr(out), _ptr(lse), _stream(stream))
+    check(st, "nvfp4kv_decode_run_static")
+    return out, lse
 
 
 def default_sm_scale(head_dim_qk: int) -> float:

@@ -23,6 +23,15 @@ cudaError_t prepare_kernel(const AttendConfig& cfg);
 using namespace nvfp4kv;
 
 namespace {
+int fail(int status, const char* fmt, ...);
+}
+
+namespace nvfp4kv {
+// Record a message for nvfp4kv_last_error_detail() and return `status`.
+int set_error_detail(int status, const char* message) { return fail(status, "%s", message); }
+}  // namespace nvfp4kv
+
+namespace {
 
 thread_local std::string g_detail;
 
