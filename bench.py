@@ -1,9 +1,10 @@
 #!/usr/bin/env python3
 """Benchmark: NVFP4 paged decode on one or more GB300s (one process per GPU).
 
-One step = the step's new K/V tokens quantised into their pages
-(nvfp4kv_quantize_append) + paged NVFP4 attention with the split-KV merge
-fused into the same kernel (nvfp4kv_decode_run) over the long-context decode
+One step = the step's new K/V tokens quantised into their pages + paged NVFP4
+attention + the split-KV merge, in one launch (nvfp4kv_decode_append_run;
+--separate-append runs nvfp4kv_quantize_append and nvfp4kv_decode_run as two
+launches instead) over the long-context decode
 workload (B=4, Hq=32, Hkv=8, D=128, kv_len=32771, page_size 16).  The plan is
 built once, outside the timed region (as serving builds it once per batch
 step and reuses it for every layer); the end-to-end leg re-plans every step.
@@ -49,15 +50,21 @@ def workload_desc(cfg: W.Workload) -> str:
                                       lens, ", causal" if cfg.causal else ""))
 
 
-def algorithmic_bytes(batch: W.Batch) -> int:
-    """KV bytes at 0.5 B/element + scale bytes + Q + O + lse + page table."""
+def algorithmic_bytes(batch: W.Batch, fused_append: bool = False) -> int:
+    """KV bytes at 0.5 B/element + scale bytes + Q + O + lse + page table;
+    with the append fused in, also the new tokens' bf16 K/V read and their
+    packed bytes + scales written."""
     c = batch.cfg
-    kv = sum(batch.kv_lens) * c.num_kv_heads * (
-        c.head_dim_qk // 2 + c.head_dim_qk // 16 + c.head_dim_vo // 2 + c.head_dim_vo // 16)
+    packed = (c.head_dim_qk // 2 + c.head_dim_qk // 16 + c.head_dim_vo // 2 +
+              c.head_dim_vo // 16)
+    kv = sum(batch.kv_lens) * c.num_kv_heads * packed
     rows = int(batch.qo_indptr[-1])
     qo = rows * c.num_qo_heads * (2 * c.head_dim_qk + 2 * c.head_dim_vo + 4)
     pt = 4 * (int(batch.kv_indices.numel()) + 2 * c.batch + 1 + c.batch + 1)
-    return kv + qo + pt
+    new = 0
+    if fused_append:
+        new = rows * c.num_kv_heads * (2 * (c.head_dim_qk + c.head_dim_vo) + packed)
+    return kv + qo + pt + new
 
 
 def measured_peak():
@@ -211,15 +218,24 @@ def run_gpu(args, world, rank, local):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    # the step's new tokens, row-aligned with the query rows
+    order = torch.argsort(batch.new.batch_idx.long() * (1 << 30) +
+                          batch.new.positions.long())
+    row_k, row_v = batch.new.k[order].to(dev), batch.new.v[order].to(dev)
+
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        N.nvfp4kv_quantize_append(cache, new_k, new_v, new_b, new_p, kv_indices, kv_indptr,
-                                  last, device_flags=flags)
-        if ev:
-            ev[1].record(stream)
-        # attention; the split-KV merge is fused into the same kernel
-        N.nvfp4kv_decode_run(plan, q, cache, kv_indices, batch.sm_scale, out=out, lse=lse)
+        if args.separate_append:
+            N.nvfp4kv_quantize_append(cache, new_k, new_v, new_b, new_p, kv_indices,
+                                      kv_indptr, last, device_flags=flags)
+            if ev:
+                ev[1].record(stream)
+        if args.separate_append:
+            N.nvfp4kv_decode_run(plan, q, cache, kv_indices, batch.sm_scale, out=out, lse=lse)
+        else:  # one launch: append fused into the attention (and the merge)
+            N.nvfp4kv_decode_append_run(plan, row_k, row_v, q, cache, kv_indices,
+                                        batch.sm_scale, out=out, lse=lse)
         if ev:
             ev[2].record(stream)
 
@@ -243,8 +259,11 @@ def run_gpu(args, world, rank, local):
         torch.cuda.synchronize()
     barrier(world)
     t_step = [e[0].elapsed_time(e[2]) for e in evs]
-    t_append = [e[0].elapsed_time(e[1]) for e in evs]
-    t_attend = [e[1].elapsed_time(e[2]) for e in evs]
+    if args.separate_append:
+        t_append = [e[0].elapsed_time(e[1]) for e in evs]
+        t_attend = [e[1].elapsed_time(e[2]) for e in evs]
+    else:  # one launch: no event between append and attention
+        t_append, t_attend = [0.0], t_step
     ms_step = statistics.mean(t_step)
     ms_step_max = max_over_ranks(ms_step, world)
     kv_tokens = sum(batch.kv_lens)
@@ -252,15 +271,13 @@ def run_gpu(args, world, rank, local):
 
     # ---- end to end through the public API with host buffers -------------
     pin = lambda t: t.contiguous().pin_memory()
-    h_q, h_k, h_v = pin(batch.q), pin(batch.new.k), pin(batch.new.v)
-    h_b, h_p = pin(batch.new.batch_idx), pin(batch.new.positions)
+    h_q, h_k, h_v = pin(batch.q), pin(batch.new.k[order]), pin(batch.new.v[order])
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(new_k), torch.empty_like(new_v)
-    d_b, d_p = torch.empty_like(new_b), torch.empty_like(new_p)
+    d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(row_k), torch.empty_like(row_v)
     ws = plan.workspace
     e2e_steps = max(3, min(args.steps, 200))
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_b, h_p))
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v))
     h2d += int(plan.info.plan_host_bytes) + 4
     d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
     times = []
@@ -268,15 +285,14 @@ def run_gpu(args, world, rank, local):
         flush.fill_(1)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_b, h_b), (d_p, h_p)):
+        for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v)):
             d.copy_(h, non_blocking=True)
         p2 = N.nvfp4kv_decode_plan(batch.qo_indptr, batch.kv_indptr, batch.last_page_len,
                                    c.num_qo_heads, c.num_kv_heads, c.head_dim_qk,
                                    c.head_dim_vo, causal=c.causal, kernel=args.kernel,
                                    device=local, reuse=plan)
-        N.nvfp4kv_quantize_append(cache, d_k, d_v, d_b, d_p, kv_indices, kv_indptr, last,
-                                  device_flags=flags)
-        N.nvfp4kv_decode_run(p2, d_q, cache, kv_indices, batch.sm_scale, out=out, lse=lse)
+        N.nvfp4kv_decode_append_run(p2, d_k, d_v, d_q, cache, kv_indices, batch.sm_scale,
+                                    out=out, lse=lse)
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
         stream.synchronize()
@@ -287,7 +303,7 @@ def run_gpu(args, world, rank, local):
 
     # ---- roofline of the attention kernel -------------------------------
     peak, peak_kind = measured_peak()
-    alg = algorithmic_bytes(batch)
+    alg = algorithmic_bytes(batch, fused_append=not args.separate_append)
     ms_attend = statistics.mean(t_attend)
     achieved = alg / (ms_attend * 1e-3) / 1e9
     traffic = traffic_per_launch(alg)
@@ -298,8 +314,9 @@ def run_gpu(args, world, rank, local):
         "dtype": "f32", "data": "synthetic",
         "config": {
             "workload": workload_desc(cfg), "layout": args.layout,
-            "step": "quantize_append(new tokens) + attention with fused split-KV merge; "
-                    "plan built once",
+            "step": ("quantize_append + decode_run (two launches)" if args.separate_append else
+                     "decode_append_run: new tokens quantised into their pages, attention and "
+                     "split-KV merge in one launch") + "; plan built once",
             "l2": "flushed between steps (512 MB write)",
             "kernel": "tensor-core mma.sync f16/f32acc" if plan.info.kernel == 1 else
                       "CUDA-core f32",
@@ -307,7 +324,8 @@ def run_gpu(args, world, rank, local):
             "chunk_pages": int(plan.info.chunk_pages),
             "us_per_call": ms_step_max * 1e3,
             "us_attend_incl_fused_merge": ms_attend * 1e3,
-            "us_append": statistics.mean(t_append) * 1e3,
+            "us_separate_append": (statistics.mean(t_append) * 1e3
+                                   if args.separate_append else None),
             "algorithmic_bytes_per_call": alg,
             "hbm_gbs_step": alg / (ms_step_max * 1e-3) / 1e9,
             "parallelism": "replicas (one independent batch per GPU)",
@@ -317,7 +335,7 @@ def run_gpu(args, world, rank, local):
                      "peak_source": peak_kind},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
-        "gpu_launches": args.steps * 2,
+        "gpu_launches": args.steps * (2 if args.separate_append else 1),
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -448,6 +466,8 @@ def main():
     ap.add_argument("--layout", default="HND", choices=["HND", "NHD"])
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 tensor-core, 2 CUDA-core")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--separate-append", action="store_true",
+                    help="quantize_append and decode_run as two launches per step")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

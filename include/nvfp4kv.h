@@ -227,6 +227,31 @@ int nvfp4kv_decode_attend(const nvfp4kv_plan_info* info, const void* q_bf16,
                           const int32_t* kv_indices, float sm_scale,
                           void* workspace, uint64_t workspace_bytes,
                           void* out_bf16, float* lse, cudaStream_t stream);
+/* One decode / extend step in one launch: the step's new tokens are
+ * quantised into their pages (the recipe of nvfp4kv_quantize_append) by the
+ * attention kernel itself, just before the pages holding them are read, then
+ * the attention runs as in nvfp4kv_decode_run.  Request b's new tokens are
+ * its last n_b positions L_b - n_b .. L_b - 1, one per query row:
+ *   new_k_bf16 [dev]  element (row, h, d) at new_k[row*k_stride_tok +
+ *                     h*k_stride_head + d] for query row `row` (the token at
+ *                     position L_b - n_b + i for row qo_indptr[b] + i), d < Dk;
+ *   new_v_bf16 [dev]  the same with the V strides, d < Dv;
+ * strides in elements, multiples of 8, 16-byte aligned.  The page table
+ * must already cover the new positions (last_page_len counts them).  The
+ * cache is written: afterwards it holds the new tokens exactly as
+ * nvfp4kv_quantize_append would have stored them.  Requires the tensor-core
+ * kernel (plan option kernel 0 or 1).  A new token whose page id is out of
+ * the pool is skipped and sets NVFP4KV_FLAG_BAD_APPEND_TARGET. */
+int nvfp4kv_decode_append_run(const nvfp4kv_plan_info* info, const void* new_k_bf16,
+                              int64_t k_stride_tok, int64_t k_stride_head,
+                              const void* new_v_bf16, int64_t v_stride_tok,
+                              int64_t v_stride_head, const void* q_bf16,
+                              int64_t q_stride_tok, int64_t q_stride_head,
+                              const nvfp4kv_paged_cache* cache,
+                              const int32_t* kv_indices, float sm_scale,
+                              void* workspace, uint64_t workspace_bytes,
+                              void* out_bf16, float* lse, cudaStream_t stream);
+
 /* Re-merge the partial states a split run left in the workspace with the
  * standalone merge kernel (nvfp4kv_merge_states over the plan's merge
  * indptr); rewrites out/lse with the same values.  A no-op without split. */

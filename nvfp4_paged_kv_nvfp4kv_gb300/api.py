@@ -18,7 +18,7 @@ from ._lib import NvFp4KvError, PagedCacheStruct, PlanInfo, PlanOptions, check
 __all__ = ["PagedCache", "Plan", "NvFp4KvError", "nvfp4kv_quantize_append",
            "nvfp4kv_decode_plan", "nvfp4kv_decode_run", "nvfp4kv_decode_attend",
            "nvfp4kv_decode_merge", "nvfp4kv_merge_states", "nvfp4kv_workspace_flags",
-           "nvfp4kv_decode_run_static"]
+           "nvfp4kv_decode_run_static", "nvfp4kv_decode_append_run"]
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -201,6 +201,22 @@ def nvfp4kv_decode_attend(plan: Plan, q: torch.Tensor, cache: PagedCache, kv_ind
                           sm_scale: float = 0.0, out=None, lse=None, stream=None):
     return _run(_lib.load().nvfp4kv_decode_attend, "nvfp4kv_decode_attend", plan, q,
                 cache, kv_indices, sm_scale, out, lse, stream)
+
+
+def nvfp4kv_decode_append_run(plan: Plan, new_k: torch.Tensor, new_v: torch.Tensor,
+                              q: torch.Tensor, cache: PagedCache, kv_indices,
+                              sm_scale: float = 0.0, out=None, lse=None, stream=None):
+    """Quantise the step's new tokens (bf16 [rows, Hkv, D], row-aligned with
+    q) into the cache and run the attention, in one launch."""
+    out, lse = _outputs(plan, out, lse, q.device)
+    s = cache.struct()
+    st = _lib.load().nvfp4kv_decode_append_run(
+        C.byref(plan.info), _ptr(new_k), new_k.stride(0), new_k.stride(1), _ptr(new_v),
+        new_v.stride(0), new_v.stride(1), _ptr(q), q.stride(0), q.stride(1), C.byref(s),
+        _ptr(kv_indices), float(sm_scale or 0.0), _ptr(plan.workspace),
+        plan.workspace.numel(), _ptr(out), _ptr(lse), _stream(stream))
+    check(st, "nvfp4kv_decode_append_run")
+    return out, lse
 
 
 def nvfp4kv_decode_merge(plan: Plan, out, lse, stream=None):

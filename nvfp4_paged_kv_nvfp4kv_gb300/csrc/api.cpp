@@ -518,14 +518,34 @@ int check_run(const nvfp4kv_plan_info* info, const void* q, int64_t qst, int64_t
 
 extern "C" {
 
-int nvfp4kv_decode_attend(const nvfp4kv_plan_info* info, const void* q_bf16,
-                          int64_t q_stride_tok, int64_t q_stride_head,
-                          const nvfp4kv_paged_cache* cache, const int32_t* kv_indices,
-                          float sm_scale, void* workspace, uint64_t workspace_bytes,
-                          void* out_bf16, float* lse, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+struct NewTokens {
+  const void* k = nullptr;
+  const void* v = nullptr;
+  int64_t k_stride_tok = 0, k_stride_head = 0, v_stride_tok = 0, v_stride_head = 0;
+};
+
+int attend(const nvfp4kv_plan_info* info, const void* q_bf16, int64_t q_stride_tok,
+           int64_t q_stride_head, const nvfp4kv_paged_cache* cache, const int32_t* kv_indices,
+           float sm_scale, void* workspace, uint64_t workspace_bytes, void* out_bf16,
+           float* lse, cudaStream_t stream, const NewTokens* nt) {
   if (int st = check_run(info, q_bf16, q_stride_tok, q_stride_head, cache, kv_indices,
                          workspace, workspace_bytes, out_bf16))
     return st;
+  if (nt) {
+    if (info->kernel != kKernelTensorCore)
+      return fail(NVFP4KV_ERR_UNSUPPORTED, "the fused append runs in the tensor-core kernel");
+    if (info->num_units > 0 &&
+        (!nt->k || !nt->v || !aligned(nt->k, 16) || !aligned(nt->v, 16) ||
+         nt->k_stride_tok % 8 || nt->k_stride_head % 8 || nt->v_stride_tok % 8 ||
+         nt->v_stride_head % 8 || nt->k_stride_tok < 0 || nt->k_stride_head < 0 ||
+         nt->v_stride_tok < 0 || nt->v_stride_head < 0))
+      return fail(NVFP4KV_ERR_INVALID_ARGUMENT,
+                  "new K/V must be 16-byte aligned with strides multiple of 8 elements");
+  }
   if (info->num_units == 0) return ok();
   AttendConfig cfg{};
   if (!lookup_kernel(info->kernel, info->head_dim_qk, info->head_dim_vo, info->rows_per_block,
@@ -555,9 +575,51 @@ int nvfp4kv_decode_attend(const nvfp4kv_plan_info* info, const void* q_bf16,
   p.partial_lse = reinterpret_cast<float*>(ws + info->off_partial_lse);
   p.counters = reinterpret_cast<int*>(ws + info->off_counters);
   p.flags = reinterpret_cast<uint32_t*>(ws + info->off_flags);
+  if (nt) {
+    p.new_k = static_cast<const uint16_t*>(nt->k);
+    p.new_v = static_cast<const uint16_t*>(nt->v);
+    p.nk_stride_tok = nt->k_stride_tok;
+    p.nk_stride_head = nt->k_stride_head;
+    p.nv_stride_tok = nt->v_stride_tok;
+    p.nv_stride_head = nt->v_stride_head;
+    p.k_global_scale = cache->k_global_scale;
+    p.v_global_scale = cache->v_global_scale;
+  }
   e = launch_attend(cfg, p, info->num_units, info->row_blocks, stream);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int nvfp4kv_decode_attend(const nvfp4kv_plan_info* info, const void* q_bf16,
+                          int64_t q_stride_tok, int64_t q_stride_head,
+                          const nvfp4kv_paged_cache* cache, const int32_t* kv_indices,
+                          float sm_scale, void* workspace, uint64_t workspace_bytes,
+                          void* out_bf16, float* lse, cudaStream_t stream) {
+  return attend(info, q_bf16, q_stride_tok, q_stride_head, cache, kv_indices, sm_scale,
+                workspace, workspace_bytes, out_bf16, lse, stream, nullptr);
+}
+
+int nvfp4kv_decode_append_run(const nvfp4kv_plan_info* info, const void* new_k_bf16,
+                              int64_t k_stride_tok, int64_t k_stride_head,
+                              const void* new_v_bf16, int64_t v_stride_tok,
+                              int64_t v_stride_head, const void* q_bf16,
+                              int64_t q_stride_tok, int64_t q_stride_head,
+                              const nvfp4kv_paged_cache* cache, const int32_t* kv_indices,
+                              float sm_scale, void* workspace, uint64_t workspace_bytes,
+                              void* out_bf16, float* lse, cudaStream_t stream) {
+  NewTokens nt;
+  nt.k = new_k_bf16;
+  nt.v = new_v_bf16;
+  nt.k_stride_tok = k_stride_tok;
+  nt.k_stride_head = k_stride_head;
+  nt.v_stride_tok = v_stride_tok;
+  nt.v_stride_head = v_stride_head;
+  return attend(info, q_bf16, q_stride_tok, q_stride_head, cache, kv_indices, sm_scale,
+                workspace, workspace_bytes, out_bf16, lse, stream, &nt);
 }
 
 int nvfp4kv_decode_merge(const nvfp4kv_plan_info* info, void* workspace,

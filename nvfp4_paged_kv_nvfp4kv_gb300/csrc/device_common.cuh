@@ -69,6 +69,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
+// order this thread's global stores before later async-proxy (bulk copy)
+// reads of the same memory
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;\n" ::: "memory");
+}
 // global -> shared bulk copy; `bytes` and both addresses are multiples of 16
 __device__ __forceinline__ void bulk_g2s(void* smem, const void* gmem, uint32_t bytes,
                                          uint64_t* bar) {

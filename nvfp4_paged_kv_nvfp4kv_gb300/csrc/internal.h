@@ -61,6 +61,13 @@ struct AttendParams {
   float* partial_lse;   // [num_partials]
   int* counters;        // [pairs * row_blocks] arrival counters (split)
   uint32_t* flags;
+  // fused append (null when not fused): bf16 K/V of the step's new tokens,
+  // row-aligned with the query rows (row qo_begin + i is position
+  // kv_len - qo_len + i), and the writable cache with its global scales
+  const uint16_t* new_k;
+  const uint16_t* new_v;
+  int64_t nk_stride_tok, nk_stride_head, nv_stride_tok, nv_stride_head;
+  float k_global_scale, v_global_scale;
 };
 
 struct AppendParams {

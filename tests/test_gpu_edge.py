@@ -200,3 +200,22 @@ def test_cuda_core_kernel(dk, dv, causal, qo_len):
     stats, g, _ = check(batch, kernel=2, force_chunk_tokens=64)
     assert g.plan.info.kernel == 2 and g.plan.info.rows_per_block == 8
     stats2, g2, _ = check(batch, kernel=2, disable_split=True)
+
+
+@pytest.mark.parametrize("layout,kw", [("HND", dict(force_chunk_tokens=32)),
+                                       ("NHD", dict(disable_split=True)),
+                                       ("HND", dict(disable_split=True))])
+@pytest.mark.parametrize("qo_len,causal", [(1, False), (7, True), (16, True)])
+def test_fused_append_small(layout, kw, qo_len, causal):
+    batch = small(kv_lens=(16, 17, 40, 161), qo_len=qo_len, causal=causal)
+    g = H.GpuCase(batch, layout=layout, append=False, **kw)
+    g.append(batch.prefix)
+    order = torch.argsort(batch.new.batch_idx.long() * (1 << 30) + batch.new.positions.long())
+    out, lse = N.nvfp4kv_decode_append_run(g.plan, batch.new.k[order].cuda(),
+                                           batch.new.v[order].cuda(), g.q, g.cache,
+                                           g.kv_indices, batch.sm_scale)
+    torch.cuda.synchronize()
+    oc, pt = H.oracle_cache(batch, layout)
+    H.compare_cache_bytes(g.cache, oc)
+    ro, rl = H.oracle_attention(batch, oc, pt)
+    H.compare(out, lse, ro, rl)

@@ -96,3 +96,33 @@ def test_forced_chunk_sweep(chunk):
     ro, rl = H.oracle_attention(batch, oc, pt) if "ref" not in _cases else _cases["ref"]
     _cases["ref"] = (ro, rl)
     H.compare(out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("name", list(W.WORKLOADS))
+def test_fused_append_run(name):
+    """nvfp4kv_decode_append_run: the step's new tokens are quantised by the
+    attention kernel itself; the cache bytes must equal the oracle's and the
+    attention must match it."""
+    batch, _, oc, pt, requests = case(name)
+    g = H.GpuCase(batch, append=False)
+    g.append(batch.prefix)
+    rows, c = int(batch.qo_indptr[-1]), batch.cfg
+    # new tokens row-aligned with the query rows: row qo_begin + i holds the
+    # token at position L_b - n_b + i
+    order = torch.argsort(batch.new.batch_idx.long() * (1 << 30) + batch.new.positions.long())
+    new_k, new_v = batch.new.k[order].cuda(), batch.new.v[order].cuda()
+    out = torch.full((rows, c.num_qo_heads, c.head_dim_vo), float("nan"), dtype=torch.bfloat16,
+                     device="cuda")
+    lse = torch.full((rows, c.num_qo_heads), float("nan"), device="cuda")
+    H.N.nvfp4kv_decode_append_run(g.plan, new_k, new_v, g.q, g.cache, g.kv_indices,
+                                  batch.sm_scale, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert H.N.nvfp4kv_workspace_flags(g.plan) == 0
+    pages = None
+    if requests is not None:
+        kvp = batch.kv_indptr.tolist()
+        pages = sorted({int(batch.kv_indices[i]) for b in requests
+                        for i in range(kvp[b], kvp[b + 1])})
+    H.compare_cache_bytes(g.cache, oc, pages)
+    ro, rl = H.oracle_attention(batch, oc, pt, requests)
+    H.compare(out, lse, ro, rl)
