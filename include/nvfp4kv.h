@@ -139,7 +139,8 @@ typedef struct nvfp4kv_plan_options {
   int32_t disable_split;      /* nonzero: one work unit per (request, head)  */
   int32_t max_splits;         /* >0: at most this many chunks per request    */
   int32_t force_chunk_tokens; /* >0: chunk size in tokens, multiple of 16    */
-  int32_t kernel;             /* 0 auto, 1 tensor-core (mma), 2 CUDA-core    */
+  int32_t kernel;             /* 0 auto, 1 tensor-core (mma.sync), 2 CUDA-core,
+                                 3 tcgen05 (head dims 128 x 128 only)      */
   int32_t num_sms;            /* >0: override the device's SM count          */
   int32_t ctas_per_sm;        /* >0: override the occupancy query            */
   int32_t reserved[5];
@@ -149,7 +150,7 @@ typedef struct nvfp4kv_plan_info {
   uint32_t magic;
   int32_t batch, num_qo_heads, num_kv_heads, head_dim_qk, head_dim_vo;
   int32_t page_size, causal;
-  int32_t kernel;          /* 1 tensor-core, 2 CUDA-core                     */
+  int32_t kernel;          /* 1 tensor-core, 2 CUDA-core, 3 tcgen05          */
   int32_t num_units;       /* attention work units (grid x)                  */
   int32_t row_blocks;      /* query-row blocks per unit (grid y)             */
   int32_t rows_per_block;  /* query rows (G x qo positions) per CTA          */
@@ -239,8 +240,8 @@ int nvfp4kv_decode_attend(const nvfp4kv_plan_info* info, const void* q_bf16,
  * strides in elements, multiples of 8, 16-byte aligned.  The page table
  * must already cover the new positions (last_page_len counts them).  The
  * cache is written: afterwards it holds the new tokens exactly as
- * nvfp4kv_quantize_append would have stored them.  Requires the tensor-core
- * kernel (plan option kernel 0 or 1).  A new token whose page id is out of
+ * nvfp4kv_quantize_append would have stored them.  Requires a tensor-core
+ * kernel (plan option kernel 0, 1 or 3).  A new token whose page id is out of
  * the pool is skipped and sets NVFP4KV_FLAG_BAD_APPEND_TARGET. */
 int nvfp4kv_decode_append_run(const nvfp4kv_plan_info* info, const void* new_k_bf16,
                               int64_t k_stride_tok, int64_t k_stride_head,

@@ -17,6 +17,7 @@
 namespace nvfp4kv {
 bool attend_config_tc(int dk, int dv, int rows, bool bulk, AttendConfig* cfg);
 bool attend_config_simt(int dk, int dv, int rows, AttendConfig* cfg);
+bool attend_config_tcgen05(int dk, int dv, int rows, AttendConfig* cfg);
 cudaError_t prepare_kernel(const AttendConfig& cfg);
 }  // namespace nvfp4kv
 
@@ -135,6 +136,7 @@ CacheView view_of(const nvfp4kv_paged_cache* c) {
 bool lookup_kernel(int kind, int dk, int dv, int rows, bool bulk, AttendConfig* cfg) {
   if (kind == kKernelTensorCore) return attend_config_tc(dk, dv, rows, bulk, cfg);
   if (kind == kKernelCudaCore) return attend_config_simt(dk, dv, rows, cfg);
+  if (kind == kKernelTcgen05) return attend_config_tcgen05(dk, dv, rows, cfg);
   return false;
 }
 
@@ -255,7 +257,7 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
                 "force_chunk_tokens %d must be a non-negative multiple of 16",
                 opts.force_chunk_tokens);
   if (opts.max_splits < 0 || opts.num_sms < 0 || opts.ctas_per_sm < 0 || opts.kernel < 0 ||
-      opts.kernel > 2)
+      opts.kernel > 3)
     return fail(NVFP4KV_ERR_INVALID_ARGUMENT, "bad plan option");
   const int G = num_qo_heads / num_kv_heads;
 
@@ -298,10 +300,13 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
   AttendConfig cfg{};
   if (kind == 0) kind = kKernelTensorCore;
   // occupancy is sized on the bulk-copy variant (the contiguous-page path)
-  if (!lookup_kernel(kind, head_dim_qk, head_dim_vo, max_rows <= 8 ? 8 : 16, true, &cfg))
+  const int want_rows = kind == kKernelTcgen05 ? std::max(max_rows, 1) : (max_rows <= 8 ? 8 : 16);
+  if (!lookup_kernel(kind, head_dim_qk, head_dim_vo, want_rows, true, &cfg))
     return fail(NVFP4KV_ERR_UNSUPPORTED, "no %s kernel for head dims (%d, %d)",
-                kind == kKernelTensorCore ? "tensor-core" : "CUDA-core", head_dim_qk,
-                head_dim_vo);
+                kind == kKernelTensorCore ? "tensor-core"
+                : kind == kKernelTcgen05  ? "tcgen05"
+                                          : "CUDA-core",
+                head_dim_qk, head_dim_vo);
   const int rows_per_block = cfg.rows;
   int num_sms = opts.num_sms, ctas_per_sm = opts.ctas_per_sm;
   if (num_sms == 0 || ctas_per_sm == 0) {
@@ -364,6 +369,9 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
     }
     if (opts.max_splits > 0)
       chunk = std::max<int64_t>(chunk, (max_np + opts.max_splits - 1) / opts.max_splits);
+    // the tcgen05 kernel streams tiles of 8 pages: whole tiles per unit
+    if (kind == kKernelTcgen05 && opts.force_chunk_tokens == 0 && chunk < max_np)
+      chunk = std::min<int64_t>((chunk + 7) / 8 * 8, max_np);
   }
   chunk = std::max<int64_t>(chunk, 1);
 
@@ -536,8 +544,8 @@ int attend(const nvfp4kv_plan_info* info, const void* q_bf16, int64_t q_stride_t
                          workspace, workspace_bytes, out_bf16))
     return st;
   if (nt) {
-    if (info->kernel != kKernelTensorCore)
-      return fail(NVFP4KV_ERR_UNSUPPORTED, "the fused append runs in the tensor-core kernel");
+    if (info->kernel != kKernelTensorCore && info->kernel != kKernelTcgen05)
+      return fail(NVFP4KV_ERR_UNSUPPORTED, "the fused append runs in the tensor-core kernels");
     if (info->num_units > 0 &&
         (!nt->k || !nt->v || !aligned(nt->k, 16) || !aligned(nt->v, 16) ||
          nt->k_stride_tok % 8 || nt->k_stride_head % 8 || nt->v_stride_tok % 8 ||

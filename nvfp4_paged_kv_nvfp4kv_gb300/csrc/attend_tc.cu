@@ -40,9 +40,9 @@
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
+#include "append_fused.cuh"
 #include "internal.h"
 #include "epilogue.cuh"
-#include "quantize.cuh"
 #include "stage.cuh"
 
 namespace nvfp4kv {
@@ -137,40 +137,7 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
     new_hi = min(u.kv_len, u.tok_begin + 16 * u.num_pages);
   }
   auto append_new = [&]() {
-    const int first_new = u.kv_len - u.qo_len;
-    constexpr int NB = DK / 16 + DV / 16;
-    for (int idx = tid; idx < (new_hi - new_lo) * NB; idx += WARPS * 32) {
-      const int tok = new_lo + idx / NB, blk = idx % NB, i = tok - first_new;
-      const bool isv = blk >= DK / 16;
-      const int jb = isv ? blk - DK / 16 : blk;
-      const uint16_t* src =
-          isv ? p.new_v + (int64_t)(u.qo_begin + i) * p.nv_stride_tok +
-                    (int64_t)u.h_kv * p.nv_stride_head
-              : p.new_k + (int64_t)(u.qo_begin + i) * p.nk_stride_tok +
-                    (int64_t)u.h_kv * p.nk_stride_head;
-      const uint4 lo16 = *reinterpret_cast<const uint4*>(src + 16 * jb);
-      const uint4 hi16 = *reinterpret_cast<const uint4*>(src + 16 * jb + 8);
-      const int32_t page = p.kv_indices[u.page_begin + (tok - u.tok_begin) / 16];
-      if (page < 0 || page >= p.cache.num_pages) {
-        atomicOr(p.flags, 0x2u);
-        continue;
-      }
-      const int slot = tok % 16;
-      uint2 packed;
-      const uint32_t sfb =
-          quantize_block16(lo16, hi16, isv ? p.v_global_scale : p.k_global_scale, &packed);
-      const CacheView& c = p.cache;
-      uint8_t* drow = const_cast<uint8_t*>(
-          isv ? c.v_data + page * c.v_sp + slot * c.v_ss + u.h_kv * c.v_sh
-              : c.k_data + page * c.k_sp + slot * c.k_ss + u.h_kv * c.k_sh);
-      uint8_t* srow = const_cast<uint8_t*>(
-          isv ? c.v_sf + page * c.vsf_sp + slot * c.vsf_ss + u.h_kv * c.vsf_sh
-              : c.k_sf + page * c.ksf_sp + slot * c.ksf_ss + u.h_kv * c.ksf_sh);
-      *reinterpret_cast<uint2*>(drow + 8 * jb) = packed;
-      srow[jb] = static_cast<uint8_t>(sfb);
-    }
-    __threadfence();
-    fence_proxy_async_global();  // before the bulk (async proxy) copies
+    append_unit_tokens<DK, DV>(p, u, new_lo, new_hi, tid, WARPS * 32);
   };
   // the prologue copies relative pages [0, WARPS * (STAGES - 1))
   const bool append_early =

@@ -17,6 +17,85 @@
 
 namespace nvfp4kv {
 
+// The split group's last CTA folds its partials.  Run by NTHREADS threads
+// (tid in [0, NTHREADS)) that synchronise with `sync`; sFin: scratch of at
+// least RB floats + 1 int.  Every thread must have stored its partials.
+template <int RB, int DV, int NTHREADS, class Sync>
+__device__ __forceinline__ void merge_if_last(const AttendParams& p, const WorkUnit& u,
+                                              int row0, int R, float* sFin, int tid,
+                                              Sync sync) {
+  using namespace dev;
+  constexpr float kLog2e = 1.44269504088896340736f;
+  const int G = p.group, Hq = p.num_qo_heads;
+  int* s_last = reinterpret_cast<int*>(sFin + 2 * RB);
+  __threadfence();
+  sync();
+  if (tid == 0) {
+    int* ctr = p.counters + (int64_t)u.pair * gridDim.y + blockIdx.y;
+    const int old = atomicAdd(ctr, 1);
+    *s_last = (old == u.num_splits - 1);
+    if (*s_last) *ctr = 0;  // every other CTA of the group has arrived
+  }
+  sync();
+  if (!*s_last) return;
+  __threadfence();
+  const int S = u.num_splits;
+  const int lane = tid & 31, warp = tid >> 5;
+  // per row: M = max lse_s, Lf = M + ln sum exp(lse_s - M)  (natural log)
+  for (int rr = warp; rr < RB; rr += NTHREADS / 32) {
+    const int r = row0 + rr;
+    if (r >= R) continue;
+    const int i = r / G, head = u.h_kv * G + r % G;
+    const float* lp = p.partial_lse + (int64_t)u.partial_base +
+                      ((int64_t)i * Hq + head) * S;
+    float M = -INFINITY;
+    for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldcg(lp + s));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float sum = 0.f;
+    if (M != -INFINITY)
+      for (int s = lane; s < S; s += 32) sum += ex2((__ldcg(lp + s) - M) * kLog2e);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) sFin[rr] = (M == -INFINITY) ? -INFINITY : M + logf(sum);
+  }
+  sync();
+  for (int idx = tid; idx < RB * (DV / 2); idx += NTHREADS) {
+    const int rr = idx / (DV / 2), d = 2 * (idx % (DV / 2));
+    const int r = row0 + rr;
+    if (r >= R) continue;
+    const int i = r / G, head = u.h_kv * G + r % G;
+    const int64_t base = (int64_t)u.partial_base + ((int64_t)i * Hq + head) * S;
+    const float Lf = sFin[rr];
+    float o0 = 0.f, o1 = 0.f;
+    if (Lf != -INFINITY) {
+      // batches of 16 partials: all loads of a batch are in flight together
+      for (int s0 = 0; s0 < S; s0 += 16) {
+        float lw[16];
+        float2 v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (s0 + j < S) {
+            lw[j] = __ldcg(p.partial_lse + base + s0 + j);
+            v[j] = __ldcg(reinterpret_cast<const float2*>(p.partial_o + (base + s0 + j) * DV + d));
+          }
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (s0 + j < S) {
+            const float w = ex2((lw[j] - Lf) * kLog2e);
+            o0 += w * v[j].x;
+            o1 += w * v[j].y;
+          }
+      }
+    }
+    const int64_t qrow = u.qo_begin + i;
+    const uint32_t packed =
+        (uint32_t)f32_to_bf16_bits(o0) | ((uint32_t)f32_to_bf16_bits(o1) << 16);
+    *reinterpret_cast<uint32_t*>(p.out + (qrow * Hq + head) * DV + d) = packed;
+    if (d == 0 && p.lse) p.lse[qrow * Hq + head] = Lf;
+  }
+}
+
 // sM/sL: [WARPS][RB] running max (log2 domain) and sum of each warp;
 // sO: [WARPS][RB][DV] each warp's un-normalised output rows;
 // sFin: scratch of at least 2*RB floats + 1 int.
@@ -27,7 +106,6 @@ __device__ __forceinline__ void finish_unit(const AttendParams& p, const WorkUni
                                             float* sFin) {
   using namespace dev;
   constexpr float kLn2 = 0.69314718055994530942f;
-  constexpr float kLog2e = 1.44269504088896340736f;
   const int tid = threadIdx.x;
   const int G = p.group, Hq = p.num_qo_heads;
   const bool partial = p.split && u.num_splits > 1;
@@ -71,74 +149,7 @@ __device__ __forceinline__ void finish_unit(const AttendParams& p, const WorkUni
   }
   if (!partial) return;
 
-  // ---- last CTA of the split group merges ------------------------------
-  int* s_last = reinterpret_cast<int*>(sFin + 2 * RB);
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    int* ctr = p.counters + (int64_t)u.pair * gridDim.y + blockIdx.y;
-    const int old = atomicAdd(ctr, 1);
-    *s_last = (old == u.num_splits - 1);
-    if (*s_last) *ctr = 0;  // every other CTA of the group has arrived
-  }
-  __syncthreads();
-  if (!*s_last) return;
-  __threadfence();
-  const int S = u.num_splits;
-  const int lane = tid & 31, warp = tid >> 5;
-  // per row: M = max lse_s, Lf = M + ln sum exp(lse_s - M)  (natural log)
-  for (int rr = warp; rr < RB; rr += WARPS) {
-    const int r = row0 + rr;
-    if (r >= R) continue;
-    const int i = r / G, head = u.h_kv * G + r % G;
-    const float* lp = p.partial_lse + (int64_t)u.partial_base +
-                      ((int64_t)i * Hq + head) * S;
-    float M = -INFINITY;
-    for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldcg(lp + s));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float sum = 0.f;
-    if (M != -INFINITY)
-      for (int s = lane; s < S; s += 32) sum += ex2((__ldcg(lp + s) - M) * kLog2e);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane == 0) sFin[rr] = (M == -INFINITY) ? -INFINITY : M + logf(sum);
-  }
-  __syncthreads();
-  for (int idx = tid; idx < RB * (DV / 2); idx += WARPS * 32) {
-    const int rr = idx / (DV / 2), d = 2 * (idx % (DV / 2));
-    const int r = row0 + rr;
-    if (r >= R) continue;
-    const int i = r / G, head = u.h_kv * G + r % G;
-    const int64_t base = (int64_t)u.partial_base + ((int64_t)i * Hq + head) * S;
-    const float Lf = sFin[rr];
-    float o0 = 0.f, o1 = 0.f;
-    if (Lf != -INFINITY) {
-      // batches of 16 partials: all loads of a batch are in flight together
-      for (int s0 = 0; s0 < S; s0 += 16) {
-        float lw[16];
-        float2 v[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (s0 + j < S) {
-            lw[j] = __ldcg(p.partial_lse + base + s0 + j);
-            v[j] = __ldcg(reinterpret_cast<const float2*>(p.partial_o + (base + s0 + j) * DV + d));
-          }
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (s0 + j < S) {
-            const float w = ex2((lw[j] - Lf) * kLog2e);
-            o0 += w * v[j].x;
-            o1 += w * v[j].y;
-          }
-      }
-    }
-    const int64_t qrow = u.qo_begin + i;
-    const uint32_t packed =
-        (uint32_t)f32_to_bf16_bits(o0) | ((uint32_t)f32_to_bf16_bits(o1) << 16);
-    *reinterpret_cast<uint32_t*>(p.out + (qrow * Hq + head) * DV + d) = packed;
-    if (d == 0 && p.lse) p.lse[qrow * Hq + head] = Lf;
-  }
+  merge_if_last<RB, DV, WARPS * 32>(p, u, row0, R, sFin, tid, [] { __syncthreads(); });
 }
 
 }  // namespace nvfp4kv

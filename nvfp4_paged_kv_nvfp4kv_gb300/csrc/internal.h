@@ -92,12 +92,12 @@ struct AppendParams {
 };
 
 // Kernel families and their launch descriptions (defined in the .cu files).
-enum KernelKind { kKernelTensorCore = 1, kKernelCudaCore = 2 };
+enum KernelKind { kKernelTensorCore = 1, kKernelCudaCore = 2, kKernelTcgen05 = 3 };
 
 struct AttendConfig {
   int kind;       // KernelKind
   int dk, dv;
-  int rows;       // rows per CTA (8 or 16)
+  int rows;       // query rows per CTA (8 or 16; 16, 32 or 64 for tcgen05)
   int warps;
   int smem_bytes;
   const void* func;  // kernel entry (for occupancy queries)

@@ -248,3 +248,26 @@ def test_merge_states_rejects():
     assert L.nvfp4kv_merge_states(buf, buf, buf, -1, 128, buf, buf, None) == 1
     assert L.nvfp4kv_merge_states(None, buf, buf, 4, 128, buf, buf, None) == 1
     assert L.nvfp4kv_merge_states(None, None, None, 0, 128, None, None, None) == 0
+
+
+@pytest.mark.parametrize("qo_len,rows", [(1, 16), (4, 16), (7, 32), (16, 64), (20, 64)])
+def test_plan_tcgen05_rows_and_tiles(qo_len, rows):
+    """kernel=3 plans N = 16 / 32 / 64 query rows per CTA (G * n rounded up,
+    64 at most) and, when it splits on its own, whole 8-page tiles per unit."""
+    batch = W.make_batch(W.custom_workload(batch=3, qo_len=qo_len, num_qo_heads=8,
+                                           num_kv_heads=2, kv_lens=(40, 3000, 9000),
+                                           causal=qo_len > 1))
+    p = plan(batch, kernel=3, ctas_per_sm=1)
+    assert p.info.kernel == 3 and p.info.rows_per_block == rows
+    assert p.info.row_blocks == -(-4 * qo_len // rows)
+    check_cover(batch, p)
+    if p.info.split:
+        max_np = int(np.diff(batch.kv_indptr.numpy()).max())
+        assert p.info.chunk_pages % 8 == 0 or p.info.chunk_pages == max_np
+
+
+def test_plan_tcgen05_rejects_other_dims():
+    batch = W.make_batch(W.custom_workload(batch=1, head_dim_qk=256, head_dim_vo=128,
+                                           kv_lens=(100,)))
+    with pytest.raises(N.NvFp4KvError):
+        plan(batch, kernel=3)
