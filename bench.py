@@ -318,8 +318,9 @@ def run_gpu(args, world, rank, local):
                      "decode_append_run: new tokens quantised into their pages, attention and "
                      "split-KV merge in one launch") + "; plan built once",
             "l2": "flushed between steps (512 MB write)",
-            "kernel": "tensor-core mma.sync f16/f32acc" if plan.info.kernel == 1 else
-                      "CUDA-core f32",
+            "kernel": {1: "tensor-core mma.sync f16/f32acc",
+                       2: "CUDA-core f32",
+                       3: "tcgen05.mma f16/f32acc, K_hat in tensor memory"}[plan.info.kernel],
             "split_units": int(plan.info.num_units), "split": int(plan.info.split),
             "chunk_pages": int(plan.info.chunk_pages),
             "us_per_call": ms_step_max * 1e3,
@@ -464,7 +465,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="long_context_decode", choices=list(W.WORKLOADS))
     ap.add_argument("--layout", default="HND", choices=["HND", "NHD"])
-    ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 tensor-core, 2 CUDA-core")
+    ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 tensor-core mma.sync, 2 CUDA-core, 3 tcgen05")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--separate-append", action="store_true",
                     help="quantize_append and decode_run as two launches per step")

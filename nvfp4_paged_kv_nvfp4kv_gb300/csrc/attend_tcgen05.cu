@@ -11,32 +11,34 @@
 //
 // One CTA = one work unit (request, kv head, chunk of pages) x a block of N
 // query rows (N = 16, 32 or 64; the G heads of the group times the query
-// positions, padded).  Tiles of 128 tokens (8 pages) pass through four warp
-// roles:
-//  * loader (warp 9): 16-byte cp.async copies of the tile's packed rows and
-//    scale rows into a ring of RS stages (any byte strides); a row's four
-//    16-byte chunks are rotated by (row / 2) % 4 so that the dequant threads'
-//    row reads hit distinct banks.  Completion: cp.async.mbarrier.arrive.
-//  * dequant (warps 4-7, thread = token): e2m1 -> f16 (cvt.rn.f16x2.e2m1x2)
-//    times the E4M3 block scale (exact in f16).  K_hat goes to tensor memory
-//    (lane = token, two dims per 32-bit column): the A operand of the score
-//    product.  V_hat goes to shared memory in the 128-byte-swizzled operand
-//    layout.
-//  * MMA (warp 8, one thread): S^T = K_hat . Q^T (M = 128 tokens, N rows,
-//    K = Dk; A from tensor memory, B = Q in shared memory) into one of two
-//    tensor-memory tiles; O^T += V_hat^T . P^T (M = 128 value dims, N rows,
-//    K = 128 tokens; both operands MN-major in shared memory) accumulated in
-//    tensor memory over the unit.  tcgen05.commit signals each product.
-//  * softmax (warps 0-3, thread = token): reads its S^T row (tcgen05.ld),
-//    p = 2^(x - m) written as the f16 P^T operand, per-row partial sums kept
-//    per thread and added up once at the end.
+// positions, padded).  Tiles of 128 tokens (8 pages) pass through three
+// roles; warp w works on tensor-memory lanes 32 (w % 4) .. + 31:
+//  * dequant (warps 8-15; thread = token, one half of the head dims): each
+//    thread copies its own token's packed bytes and scale bytes RS - 1 tiles
+//    ahead (cp.async groups, no cross-thread hand-off), then e2m1 -> f16
+//    (cvt.rn.f16x2.e2m1x2) times the E4M3 block scale (exact in f16).  K_hat
+//    goes to tensor memory (lane = token, two dims per 32-bit column): the A
+//    operand of the score product.  V_hat goes to shared memory in the
+//    128-byte-swizzled operand layout.  Three K_hat / V_hat buffers.
+//  * softmax (warps 0-7; thread = token for S^T, = value dim for O^T, one
+//    half of the query-row columns): tcgen05.ld of its S^T row, p = 2^(x - m)
+//    written as the f16 P^T operand, per-row partial sums kept per thread and
+//    added up once at the end.
+//  * product issue (warp 16, one thread): S^T = K_hat . Q^T (M = 128 tokens,
+//    N rows, K = Dk; A from tensor memory, B = Q in shared memory) into one
+//    of two tensor-memory tiles, and O^T += V_hat^T . P^T (M = 128 value
+//    dims, N rows, K = 128 tokens; both operands MN-major in shared memory)
+//    accumulated in tensor memory over the unit, each as soon as its inputs
+//    are ready; tcgen05.commit signals them on mbarriers.  One thread can
+//    issue a product about every 54 cycles, whatever N, so this layout suits
+//    many query rows per kv head (extend); decode keeps the mma.sync kernel.
 // Putting the tile's tokens on the M side fills the 128-row MMA even for a
 // handful of query rows.  The running row maximum m is raised only when a
 // score exceeds it by more than 2^8 (or the row has none yet): then the
 // exact tile maximum is taken and O and the partial sums are rescaled;
 // otherwise p <= 2^8 fits f16 and no cross-thread reduction is needed.
 // Every wait is bounded; a wait that runs out sets flag 0x4 and the CTA
-// winds down (waiting, bounded, for its own copies and products first).
+// winds down (its copies and products in flight complete first).
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -53,9 +55,12 @@ using namespace dev;
 
 constexpr int kTileTok = 128;
 constexpr int kTilePages = kTileTok / kPageSize;
-constexpr int kThreads = 320;  // softmax 0-3, dequant 4-7, MMA 8, loader 9
+constexpr int kThreads = 544;  // softmax warps 0-7, dequant warps 8-15, issue warp 16
+constexpr int kKB = 3;         // K_hat / V_hat buffers
 constexpr float kRaise = 8.f;  // log2 of the largest p before m is raised
-constexpr uint32_t kSpin = 1u << 22;
+constexpr uint32_t kSleepNs = 20000;  // suspend hint of one poll
+constexpr uint32_t kPolls = 50000;    // polls before a wait gives up
+constexpr uint32_t kIdlePolls = 1u << 21;  // idle rounds of the product issuer
 
 // ---- tensor memory, tcgen05 and barrier helpers (inline PTX) -------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
@@ -91,6 +96,24 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
         "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+// NC consecutive columns (a multiple of 8) of this thread's lane
+template <int NC>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t* r) {
+  static_assert(NC % 8 == 0, "columns");
+  if constexpr (NC % 16 == 0) {
+#pragma unroll
+    for (int c = 0; c < NC / 16; ++c) tmem_ld16(taddr + 16 * c, r + 16 * c);
+  } else {
+#pragma unroll
+    for (int c = 0; c < NC / 8; ++c) tmem_ld8(taddr + 8 * c, r + 8 * c);
+  }
+}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
@@ -99,6 +122,24 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
       "r"(r[15])
       : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
+template <int NC>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t* r) {
+  static_assert(NC % 8 == 0, "columns");
+  if constexpr (NC % 16 == 0) {
+#pragma unroll
+    for (int c = 0; c < NC / 16; ++c) tmem_st16(taddr + 16 * c, r + 16 * c);
+  } else {
+#pragma unroll
+    for (int c = 0; c < NC / 8; ++c) tmem_st8(taddr + 8 * c, r + 8 * c);
+  }
 }
 // Wait for outstanding tcgen05.ld and make their results the registers'
 // current values for the code that follows.
@@ -154,10 +195,16 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_addr(bar)) : "memory");
 }
-// one arrival on `bar` once this thread's earlier cp.async copies landed
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_addr(bar))
-               : "memory");
+// non-blocking test of a phase
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
@@ -182,11 +229,25 @@ __device__ __forceinline__ bool named_and(int id, int n, bool v) {
       : "memory");
   return r != 0;
 }
-// Bounded wait; gives up early once another thread of the CTA gave up.
+// One poll that may suspend the thread until the phase completes (or the
+// hinted time, in ns, elapses): waiting warps sleep instead of spinning and
+// leave the issue slots to the warps that work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kSleepNs)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait (at least kPolls polls, at most kPolls * kSleepNs ns); gives
+// up early once another thread of the CTA gave up.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort,
                                          uint32_t* flags) {
-  for (uint32_t it = 0; it < kSpin; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+  for (uint32_t it = 0; it < kPolls; ++it) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
     if (*abort) return false;
   }
   *abort = 1;
@@ -196,8 +257,8 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
 // Bounded wait that ignores the abort flag (the wind-down of copies and
 // products in flight).
 __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, uint32_t* flags) {
-  for (uint32_t it = 0; it < kSpin; ++it)
-    if (mbar_try_wait(bar, parity)) return;
+  for (uint32_t it = 0; it < kPolls; ++it)
+    if (mbar_try_wait_sleep(bar, parity)) return;
   atomicOr(flags, 0x4u);
 }
 // order-preserving float <-> int keys (for integer max reductions)
@@ -212,30 +273,32 @@ __device__ __forceinline__ float funkey(int k) {
 template <int N>
 struct Tg5 {
   static constexpr int DK = 128, DV = 128;
-  static constexpr int RS = 4;                          // packed stages
-  static constexpr int PAGE = 1024 + 128 + 1024 + 128;  // K, K scales, V, V scales
-  static constexpr int RAW = kTilePages * PAGE;
-  static constexpr int VH = kTileTok * DV * 2;          // one V_hat tile (f16)
-  static constexpr int PB = kTileTok * N * 2;           // one P^T tile (f16)
-  static constexpr int ROWB = N * 2;                    // P bytes per token
+  static constexpr int NH = N / 2;                    // columns per softmax thread
+  static constexpr int RS = N == 64 ? 3 : 4;          // copy stages per dequant thread
+  static constexpr int WST = 2304;                    // one dequant warp's stage
+  static constexpr int STAGE = 8 * WST;               // 8 pages of K, V and scales
+  static constexpr int VH = kTileTok * DV * 2;        // one V_hat tile (f16)
+  static constexpr int PB = kTileTok * N * 2;         // one P^T tile (f16)
+  static constexpr int ROWB = N * 2;                  // P bytes per token
   static constexpr uint32_t PSWZ = N == 16 ? kSwz32 : N == 32 ? kSwz64 : kSwz128;
   static constexpr int PSWB = N == 16 ? 1 : N == 32 ? 2 : 3;  // swizzle bits
   static constexpr int QB = N * DK * 2;
   static constexpr int OFF_V = 0;
-  static constexpr int OFF_P = OFF_V + 2 * VH;
+  static constexpr int OFF_P = OFF_V + kKB * VH;
   static constexpr int OFF_Q = OFF_P + 2 * PB;
   static constexpr int OFF_RAW = OFF_Q + QB;
-  static constexpr int OFF_MISC = OFF_RAW + RS * RAW;
+  static constexpr int OFF_MISC = OFF_RAW + RS * STAGE;
   static constexpr int MISC = 8192;
   static constexpr int SMEM = OFF_MISC + MISC + 1024;  // + alignment slack
-  // tensor memory columns: K_hat x2 (64 each), S^T x2 (N each), O^T (N)
-  static constexpr int KCOL = 0, SCOL = 128, OCOL = 128 + 2 * N;
+  // tensor memory columns: K_hat x3 (64 each), S^T x2 (N each), O^T (N)
+  static constexpr int KCOL = 0, SCOL = 64 * kKB, OCOL = SCOL + 2 * N;
   static constexpr int TCOLS = (OCOL + N) <= 256 ? 256 : 512;
   static constexpr uint32_t IDESC_QK = idesc_f16(128, N, 0, 0);
   static constexpr uint32_t IDESC_PV = idesc_f16(128, N, 1, 1);
   static_assert(OFF_P % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_RAW % 1024 == 0, "align");
-  static_assert(RAW % 16 == 0 && OFF_MISC % 16 == 0, "align");
+  static_assert(STAGE % 1024 == 0 && OFF_MISC % 16 == 0, "align");
   static_assert(OCOL + N <= TCOLS, "tensor memory");
+  static_assert(SMEM <= 232448, "shared memory");
 };
 
 // swizzled byte offset inside a 1024-byte-aligned operand region (the
@@ -248,7 +311,9 @@ __device__ __forceinline__ uint32_t swz(uint32_t off) {
 template <int N>
 __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const AttendParams p) {
   using T = Tg5<N>;
-  constexpr int DK = T::DK, DV = T::DV, RS = T::RS;
+  constexpr int DK = T::DK, DV = T::DV, RS = T::RS, NH = T::NH;
+  constexpr int CW = NH < 16 ? NH : 16;  // columns per softmax chunk
+  constexpr int NCH = NH / CW;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -257,26 +322,27 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
   uint8_t* sQ = smem + T::OFF_Q;
   uint8_t* sRaw = smem + T::OFF_RAW;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::OFF_MISC);
-  uint64_t* raw_full = bars;               // [RS] loader -> dequant
-  uint64_t* raw_empty = bars + RS;         // [RS] dequant -> loader
-  uint64_t* kv_full = bars + 2 * RS;       // [2] dequant -> MMA
-  uint64_t* kv_empty = bars + 2 * RS + 2;  // [2] MMA -> dequant
-  uint64_t* s_full = bars + 2 * RS + 4;    // [2] MMA -> softmax
-  uint64_t* p_full = bars + 2 * RS + 6;    // [2] softmax -> MMA
-  uint64_t* pv_done = bars + 2 * RS + 8;   // [2] MMA -> softmax
-  uint64_t* q_full = bars + 2 * RS + 10;   // softmax -> MMA
-  uint64_t* fin = bars + 2 * RS + 11;      // MMA wind-down
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * RS + 12);
+  uint64_t* kv_full = bars;        // [3] dequant -> MMA issue
+  uint64_t* kv_empty = bars + 3;   // [3] PV done -> dequant
+  uint64_t* s_full = bars + 6;     // [2] QK done -> softmax
+  uint64_t* p_full = bars + 8;     // [2] softmax -> MMA issue
+  uint64_t* pv_done = bars + 10;   // [2] PV done -> softmax
+  uint64_t* q_full = bars + 12;    // Q block ready -> MMA issue
+  uint64_t* fin = bars + 13;       // wind-down of the products
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int* s_minlim = reinterpret_cast<int*>(s_tmem + 2);
-  float4* s_rowp = reinterpret_cast<float4*>(s_tmem + 4);  // [N] {f, -m_use, thr, lim}
-  float* s_m = reinterpret_cast<float*>(s_rowp + N);        // [N] running max (log2)
-  int* s_max = reinterpret_cast<int*>(s_m + N);             // [N] reduction keys
-  float* s_delta = reinterpret_cast<float*>(s_max + N);     // [N]
-  float* s_corr = s_delta + N;                              // [N]
-  int* s_qamax = reinterpret_cast<int*>(s_corr + N);        // [N]
-  float* s_l = reinterpret_cast<float*>(s_qamax + N);       // [4][N]
-  float* s_fin = s_l + 4 * N;                               // [2N + 1]
+  // per query-row column: score factor, -m_use, raise threshold, causal limit
+  float* s_f = reinterpret_cast<float*>(s_tmem + 4);
+  float* s_nm = s_f + N;
+  float* s_thr = s_nm + N;
+  int* s_lim = reinterpret_cast<int*>(s_thr + N);
+  float* s_m = reinterpret_cast<float*>(s_lim + N);     // running max (log2)
+  int* s_max = reinterpret_cast<int*>(s_m + N);         // reduction keys
+  float* s_corr = reinterpret_cast<float*>(s_max + N);
+  int* s_qamax = reinterpret_cast<int*>(s_corr + N);
+  float* s_l = reinterpret_cast<float*>(s_qamax + N);   // [4][N]
+  float* s_fin = s_l + 4 * N;                           // [2N + 1]
 
   const WorkUnit u = p.units[blockIdx.x];
   const int G = p.group;
@@ -284,29 +350,30 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
   const int row0 = blockIdx.y * N;
   if (row0 >= R) return;  // uniform: before any barrier or tensor memory use
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q4 = warp & 3;                        // tensor-memory lane quarter
+  const int j = 32 * q4 + lane;                   // token of the tile / value dim
+  const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
   const int ntiles = (u.num_pages + kTilePages - 1) / kTilePages;
   const int tok_end = min(u.kv_len, u.tok_begin + kPageSize * u.num_pages);
 
   if (tid == 0) {
-    for (int s = 0; s < RS; ++s) {
-      mbar_init(&raw_full[s], 32);
-      mbar_init(&raw_empty[s], 4);
+    for (int b = 0; b < kKB; ++b) {
+      mbar_init(&kv_full[b], 8);
+      mbar_init(&kv_empty[b], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&kv_full[b], 4);
-      mbar_init(&kv_empty[b], 1);
       mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], 4);
+      mbar_init(&p_full[b], 8);
       mbar_init(&pv_done[b], 1);
     }
-    mbar_init(q_full, 4);
+    mbar_init(q_full, 8);
     mbar_init(fin, 1);
     mbar_init_fence();
     *s_abort = 0;
     *s_minlim = INT32_MAX;
   }
   if (tid < N) s_qamax[tid] = 0;
-  if (warp == 8) {
+  if (warp == 0) {
     tmem_alloc(s_tmem, T::TCOLS);
     tmem_relinquish();
   }
@@ -321,82 +388,63 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  if (warp == 9) {
-    // ================= loader =================
+  if (warp >= 8 && warp < 16) {
+    // ================= dequant (thread = token, half the dims) ===========
     const CacheView& c = p.cache;
-    const int32_t* pidx = p.kv_indices + u.page_begin;
-    const int r_lo = lane >> 2, ch = lane & 3;  // row (mod 8) and chunk of this lane
-    int issued = 0;
-    for (int i = 0; i < ntiles; ++i) {
-      const int s = i % RS;
-      if (i >= RS) {
-        const bool ok = __all_sync(0xffffffffu,
-                                   wait_bar(&raw_empty[s], ((i / RS) - 1) & 1, s_abort, p.flags));
-        if (!ok) break;
+    const int hd = (warp - 8) >> 2;  // dims [64 hd, 64 hd + 64)
+    const int slot = j & 15;
+    uint8_t* wst = sRaw + (warp - 8) * T::WST;
+    // stage layout per warp: K chunks [2][32][16], V chunks [2][32][16],
+    // K scales [32][4], V scales [32][4]
+    auto issue = [&](int t) {
+      const int pg = t * kTilePages + (j >> 4);
+      if (pg >= u.num_pages) return;
+      int32_t pid = p.kv_indices[u.page_begin + pg];
+      if (pid < 0 || pid >= c.num_pages) {
+        atomicOr(p.flags, 0x1u);
+        pid = 0;
       }
-      const int np_t = min(kTilePages, u.num_pages - i * kTilePages);
-      int32_t pid = 0;
-      if (lane < np_t) {
-        pid = pidx[i * kTilePages + lane];
-        if (pid < 0 || pid >= c.num_pages) {
-          atomicOr(p.flags, 0x1u);
-          pid = 0;
-        }
-      }
-      uint8_t* st = sRaw + s * T::RAW;
+      uint8_t* st = wst + (t % RS) * T::STAGE;
+      const uint8_t* kr = c.k_data + pid * c.k_sp + u.h_kv * c.k_sh + slot * c.k_ss + 32 * hd;
+      const uint8_t* vr = c.v_data + pid * c.v_sp + u.h_kv * c.v_sh + slot * c.v_ss + 32 * hd;
+      cp_async_16(st + lane * 16, kr);
+      cp_async_16(st + 512 + lane * 16, kr + 16);
+      cp_async_16(st + 1024 + lane * 16, vr);
+      cp_async_16(st + 1536 + lane * 16, vr + 16);
+      cp_async_small<4>(st + 2048 + lane * 4,
+                        c.k_sf + pid * c.ksf_sp + u.h_kv * c.ksf_sh + slot * c.ksf_ss + 4 * hd);
+      cp_async_small<4>(st + 2176 + lane * 4,
+                        c.v_sf + pid * c.vsf_sp + u.h_kv * c.vsf_sh + slot * c.vsf_ss + 4 * hd);
+    };
 #pragma unroll
-      for (int q = 0; q < kTilePages; ++q) {
-        const int32_t pq = __shfl_sync(0xffffffffu, pid, q);
-        if (q >= np_t) break;
-        uint8_t* pg = st + q * T::PAGE;
-        const uint8_t* kb = c.k_data + pq * c.k_sp + u.h_kv * c.k_sh;
-        const uint8_t* vb = c.v_data + pq * c.v_sp + u.h_kv * c.v_sh;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int slot = r_lo + 8 * half;  // 0..15
-          const int row = 16 * q + slot;     // token of the tile
-          const int pos = (ch ^ ((row >> 1) & 3)) << 4;
-          cp_async_16(pg + slot * 64 + pos, kb + slot * c.k_ss + ch * 16);
-          cp_async_16(pg + 1152 + slot * 64 + pos, vb + slot * c.v_ss + ch * 16);
-        }
-        if (lane < 16) {
-          cp_async_small<8>(pg + 1024 + lane * 8,
-                            c.k_sf + pq * c.ksf_sp + u.h_kv * c.ksf_sh + lane * c.ksf_ss);
-        } else {
-          const int sl = lane - 16;
-          cp_async_small<8>(pg + 2176 + sl * 8,
-                            c.v_sf + pq * c.vsf_sp + u.h_kv * c.vsf_sh + sl * c.vsf_ss);
-        }
-      }
-      cp_async_arrive(&raw_full[s]);
-      issued = i + 1;
+    for (int t = 0; t < RS - 1; ++t) {
+      if (t < ntiles) issue(t);
+      cp_async_commit();
     }
-    // wind-down: every copy issued has landed before the CTA may exit
-    for (int i = max(0, issued - RS); i < issued; ++i)
-      drain_bar(&raw_full[i % RS], (i / RS) & 1, p.flags);
-  } else if (warp >= 4 && warp < 8) {
-    // ================= dequant (thread = token) =================
-    const int j = tid - 128;  // token of the tile; tensor-memory lane
-    const int slot = j & 15, rot = (j >> 1) & 3;
-    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     for (int i = 0; i < ntiles; ++i) {
-      const int s = i % RS, b = i & 1;
-      bool ok = wait_bar(&raw_full[s], (i / RS) & 1, s_abort, p.flags);
-      if (ok && i >= 2) ok = wait_bar(&kv_empty[b], ((i >> 1) - 1) & 1, s_abort, p.flags);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      if (i + RS - 1 < ntiles) issue(i + RS - 1);
+      cp_async_commit();
+      cp_async_wait<RS - 1>();  // this thread's copies of tile i landed
+      const int bi = i % kKB;
+      if (i >= kKB) {
+        // one lane polls; the others sleep in the shuffle
+        bool ok = true;
+        if (lane == 0) ok = wait_bar(&kv_empty[bi], ((i / kKB) - 1) & 1, s_abort, p.flags);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      }
       tc_fence_after();
       const bool valid = u.tok_begin + i * kTileTok + j < tok_end;
-      const uint8_t* pg = sRaw + s * T::RAW + (j >> 4) * T::PAGE;
-      // ---- K_hat row -> tensor memory columns [64 b, 64 b + 64) ----------
+      const uint8_t* st = wst + (i % RS) * T::STAGE;
+      // ---- K_hat: tensor memory columns 64 bi + 32 hd + [0, 32) -----------
       {
-        const uint2 sf = *reinterpret_cast<const uint2*>(pg + 1024 + slot * 8);
+        const uint32_t sf = *reinterpret_cast<const uint32_t*>(st + 2048 + lane * 4);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const uint4 w = *reinterpret_cast<const uint4*>(pg + slot * 64 + ((cc ^ rot) << 4));
-          const uint32_t s2 = e4m3x2_to_f16x2(((cc < 2 ? sf.x : sf.y) >> (16 * (cc & 1))));
+        for (int cc = 0; cc < 2; ++cc) {
+          const uint4 w = *reinterpret_cast<const uint4*>(st + cc * 512 + lane * 16);
+          const uint32_t s2 = e4m3x2_to_f16x2(sf >> (16 * cc));
           const uint32_t slo = bcast_lo(s2), shi = bcast_hi(s2);
-          uint32_t kr[16];
           const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+          uint32_t kr[16];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint32_t h[4];
@@ -404,19 +452,18 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
 #pragma unroll
             for (int e = 0; e < 4; ++e) kr[4 * q + e] = hmul2(h[e], q < 2 ? slo : shi);
           }
-          tmem_st16(tmem + lane_base + T::KCOL + 64 * b + 16 * cc, kr);
+          tmem_st16(tmem + lane_base + T::KCOL + 64 * bi + 32 * hd + 16 * cc, kr);
         }
       }
-      // ---- V_hat row -> shared memory (MN-major operand layout) ---------
+      // ---- V_hat: shared memory, 64-dim block hd (MN-major operand) -------
       {
-        uint2 sf = *reinterpret_cast<const uint2*>(pg + 2176 + slot * 8);
-        if (!valid) sf = make_uint2(0u, 0u);  // no stale byte can poison 0 * NaN
-        uint8_t* vt = sV + b * T::VH;
+        // no stale scale byte of a slot past the end can poison 0 * NaN
+        const uint32_t sf = valid ? *reinterpret_cast<const uint32_t*>(st + 2176 + lane * 4) : 0u;
+        uint8_t* vt = sV + bi * T::VH + hd * (kTileTok * 128);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const uint4 w =
-              *reinterpret_cast<const uint4*>(pg + 1152 + slot * 64 + ((cc ^ rot) << 4));
-          const uint32_t s2 = e4m3x2_to_f16x2(((cc < 2 ? sf.x : sf.y) >> (16 * (cc & 1))));
+        for (int cc = 0; cc < 2; ++cc) {
+          const uint4 w = *reinterpret_cast<const uint4*>(st + 1024 + cc * 512 + lane * 16);
+          const uint32_t s2 = e4m3x2_to_f16x2(sf >> (16 * cc));
           const uint32_t slo = bcast_lo(s2), shi = bcast_hi(s2);
           const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -424,9 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
             uint32_t h[4];
             e2m1x8_to_f16x8(ww[q], h);
             const uint32_t sc = q < 2 ? slo : shi;
-            // dims 32cc + 8q .. +7: 64-dim block cc/2, 16-byte chunk 4(cc&1)+q
-            const uint32_t off = (uint32_t)(cc >> 1) * (kTileTok * 128) + (j >> 3) * 1024 +
-                                 (j & 7) * 128 + (4 * (cc & 1) + q) * 16;
+            const uint32_t off = (j >> 3) * 1024 + (j & 7) * 128 + (4 * cc + q) * 16;
             *reinterpret_cast<uint4*>(vt + swz<3>(off)) =
                 make_uint4(hmul2(h[0], sc), hmul2(h[1], sc), hmul2(h[2], sc), hmul2(h[3], sc));
           }
@@ -436,47 +481,68 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&kv_full[b]);
-        mbar_arrive(&raw_empty[s]);
-      }
+      if (lane == 0) mbar_arrive(&kv_full[bi]);
     }
-  } else if (warp == 8) {
-    // ================= MMA issue (one thread) =================
+    cp_async_wait<0>();
+  } else if (warp == 16) {
+    // ================= product issue (one thread) =========================
     if (lane == 0) {
-      const uint32_t q_base = smem_addr(sQ), v_base = smem_addr(sV), p_base = smem_addr(sP);
-      auto qk = [&](int i) -> bool {
-        const int b = i & 1;
-        if (!wait_bar(&kv_full[b], (i >> 1) & 1, s_abort, p.flags)) return false;
+      // descriptors of the first k-step; later k-steps advance the start
+      // address field (16-byte units) by constant offsets
+      const uint64_t qd0 = smem_desc(smem_addr(sQ), 16, 1024, kSwz128);
+      const uint64_t vd0 = smem_desc(smem_addr(sV), kTileTok * 128, 1024, kSwz128);
+      const uint64_t pd0 = smem_desc(smem_addr(sP), T::PB, 8 * T::ROWB, T::PSWZ);
+      auto issue_qk = [&](int k) {
         tc_fence_after();
+        const int bi = k % kKB, sb = k & 1;
+        const uint32_t d = tmem + T::SCOL + N * sb, a = tmem + T::KCOL + 64 * bi;
 #pragma unroll
-        for (int k = 0; k < DK / 16; ++k) {
-          const uint64_t bd =
-              smem_desc(q_base + (k >> 2) * (N * 128) + (k & 3) * 32, 16, 1024, kSwz128);
-          umma_ts(tmem + T::SCOL + N * b, tmem + T::KCOL + 64 * b + 8 * k, bd, T::IDESC_QK,
-                  k > 0 ? 1u : 0u);
-        }
-        umma_commit(&s_full[b]);
-        return true;
+        for (int kk = 0; kk < DK / 16; ++kk)
+          umma_ts(d, a + 8 * kk, qd0 + (((kk >> 2) * (N * 128) + (kk & 3) * 32) >> 4),
+                  T::IDESC_QK, kk > 0 ? 1u : 0u);
+        umma_commit(&s_full[sb]);
       };
-      bool ok = wait_bar(q_full, 0, s_abort, p.flags);
-      tc_fence_after();
-      if (ok && ntiles > 0) ok = qk(0);
-      for (int i = 0; ok && i < ntiles; ++i) {
-        if (i + 1 < ntiles && !qk(i + 1)) break;
-        const int b = i & 1;
-        if (!wait_bar(&p_full[b], (i >> 1) & 1, s_abort, p.flags)) break;
+      auto issue_pv = [&](int i) {
         tc_fence_after();
+        const int bi = i % kKB, sb = i & 1;
+        const uint64_t vd = vd0 + ((bi * T::VH) >> 4), pd = pd0 + ((sb * T::PB) >> 4);
+        umma_ss(tmem + T::OCOL, vd, pd, T::IDESC_PV, i > 0 ? 1u : 0u);
 #pragma unroll
-        for (int k = 0; k < kTileTok / 16; ++k) {
-          const uint64_t ad =
-              smem_desc(v_base + b * T::VH + k * 2048, kTileTok * 128, 1024, kSwz128);
-          const uint64_t bd = smem_desc(p_base + b * T::PB + k * 16 * T::ROWB, T::PB,
-                                        8 * T::ROWB, T::PSWZ);
-          umma_ss(tmem + T::OCOL, ad, bd, T::IDESC_PV, (i > 0 || k > 0) ? 1u : 0u);
+        for (int k = 1; k < kTileTok / 16; ++k)
+          umma_ss(tmem + T::OCOL, vd + ((k * 2048) >> 4), pd + ((k * 16 * T::ROWB) >> 4),
+                  T::IDESC_PV, 1u);
+        umma_commit(&pv_done[sb]);
+        umma_commit(&kv_empty[bi]);
+      };
+      // Issue whichever product has its inputs: S(qk) once K_hat(qk) is in
+      // and S buffer qk & 1 was consumed (PV(qk - 2) issued), O += PV(pv)
+      // once P(pv) is written.
+      bool ok = wait_bar(q_full, 0, s_abort, p.flags);
+      int qk = 0, pv = 0;
+      uint32_t idle = 0;
+      while (ok && pv < ntiles) {
+        bool prog = false;
+        if (qk < ntiles && qk < pv + 2 && mbar_test_wait(&kv_full[qk % kKB], (qk / kKB) & 1)) {
+          issue_qk(qk);
+          ++qk;
+          prog = true;
         }
-        umma_commit(&pv_done[b]);
-        umma_commit(&kv_empty[b]);
+        if (pv < qk && mbar_test_wait(&p_full[pv & 1], (pv >> 1) & 1)) {
+          issue_pv(pv);
+          ++pv;
+          prog = true;
+        }
+        if (prog) {
+          idle = 0;
+          continue;
+        }
+        if (*s_abort) break;
+        if (++idle > kIdlePolls) {
+          *s_abort = 1;
+          atomicOr(p.flags, 0x4u);
+          break;
+        }
+        __nanosleep(32);
       }
       // wind-down: every product issued has completed
       umma_commit(fin);
@@ -484,14 +550,15 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
     }
     __syncwarp();
   } else {
-    // ================= softmax + epilogue (warps 0-3) =================
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    // ================= softmax + epilogue (warps 0-7) =====================
+    const int c0 = (warp >> 2) * NH;  // this thread's first query-row column
     // ---- Q block: bf16 -> f16 times a power of two per row, swizzled ------
     constexpr int QCH = N * DK / 8;  // 16-byte chunks of f16
-    uint4 qv[QCH / 128];
+    constexpr int QPT = QCH / 256;
+    uint4 qv[QPT];
 #pragma unroll
-    for (int k = 0; k < QCH / 128; ++k) {
-      const int ci = tid + 128 * k, r = ci / (DK / 8), c8 = ci % (DK / 8), gr = row0 + r;
+    for (int k = 0; k < QPT; ++k) {
+      const int ci = tid + 256 * k, r = ci / (DK / 8), c8 = ci % (DK / 8), gr = row0 + r;
       qv[k] = make_uint4(0u, 0u, 0u, 0u);
       if (gr < R)
         qv[k] = *reinterpret_cast<const uint4*>(
@@ -505,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
                              fabsf(bf16_bits_to_f32(w[e] >> 16))));
       atomicMax(&s_qamax[r], __float_as_int(am));
     }
-    named_sync(1, 128);
+    named_sync(1, 256);
     auto exp_of = [&](int r) {  // e with amax * 2^e in [2^14, 2^15)
       const float amax = __int_as_float(s_qamax[r]);
       int e = 0;
@@ -513,8 +580,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
       return max(-120, min(120, e));
     };
 #pragma unroll
-    for (int k = 0; k < QCH / 128; ++k) {
-      const int ci = tid + 128 * k, r = ci / (DK / 8), c8 = ci % (DK / 8);
+    for (int k = 0; k < QPT; ++k) {
+      const int ci = tid + 256 * k, r = ci / (DK / 8), c8 = ci % (DK / 8);
       const float up = __uint_as_float((uint32_t)(127 + exp_of(r)) << 23);
       const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
       uint32_t h[4];
@@ -528,183 +595,229 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
     }
     if (tid < N) {
       const int r = tid, gr = row0 + r;
-      float4 rp;
       if (gr < R) {
         const int lim = p.causal ? (u.kv_len - u.qo_len + gr / G) : (u.kv_len - 1);
-        rp = make_float4(p.qk_scale_log2 * __uint_as_float((uint32_t)(127 - exp_of(r)) << 23),
-                         0.f, -INFINITY, __int_as_float(lim));
+        s_f[r] = p.qk_scale_log2 * __uint_as_float((uint32_t)(127 - exp_of(r)) << 23);
+        s_nm[r] = 0.f;
+        s_thr[r] = -INFINITY;  // no maximum yet: any visible score raises
+        s_lim[r] = lim;
         atomicMin(s_minlim, lim);
       } else {  // padding row: every score -inf, never raises
-        rp = make_float4(0.f, -INFINITY, INFINITY, __int_as_float(-1));
+        s_f[r] = 0.f;
+        s_nm[r] = -INFINITY;
+        s_thr[r] = INFINITY;
+        s_lim[r] = -1;
       }
-      s_rowp[r] = rp;
       s_m[r] = -INFINITY;
     }
     fence_async_smem();
-    named_sync(1, 128);
+    named_sync(1, 256);
     __syncwarp();
     if (lane == 0) mbar_arrive(q_full);
     const int min_lim = *s_minlim;
+    const int nvalid = min(N, R - row0);  // columns that are real query rows
+    const bool active = c0 < nvalid;      // warp-uniform
 
-    float lpart[N];
+    // x = log2-domain score relative to the running max, -inf where masked
+    auto scores = [&](int ch, int sb, bool tok_ok, bool mask_rows, int tok, float (&x)[CW]) {
+      uint32_t sv[CW];
+      tmem_ld<CW>(tmem + lane_base + T::SCOL + N * sb + c0 + ch * CW, sv);
+      tmem_wait_ld<CW>(sv);
+      const int cb = c0 + ch * CW;
 #pragma unroll
-    for (int r = 0; r < N; ++r) lpart[r] = 0.f;
+      for (int e4 = 0; e4 < CW; e4 += 4) {
+        const float4 f = *reinterpret_cast<const float4*>(s_f + cb + e4);
+        const float4 nm = *reinterpret_cast<const float4*>(s_nm + cb + e4);
+        const float ff[4] = {f.x, f.y, f.z, f.w}, nn[4] = {nm.x, nm.y, nm.z, nm.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          x[e4 + e] = tok_ok ? fmaf(__uint_as_float(sv[e4 + e]), ff[e], nn[e]) : -INFINITY;
+        if (mask_rows) {
+          const int4 lm = *reinterpret_cast<const int4*>(s_lim + cb + e4);
+          const int ll[4] = {lm.x, lm.y, lm.z, lm.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (tok > ll[e]) x[e4 + e] = -INFINITY;
+        }
+      }
+    };
+
+    float lpart[NH];
+#pragma unroll
+    for (int r = 0; r < NH; ++r) lpart[r] = 0.f;
     bool alive = true;
     for (int i = 0; i < ntiles; ++i) {
-      const int b = i & 1;
-      // S(i) done also means PV(i-2) done: P buffer b is free again
-      alive = named_and(1, 128, wait_bar(&s_full[b], (i >> 1) & 1, s_abort, p.flags));
+      const int sb = i & 1;
+      // thread 0 polls; the group sleeps in the barrier that shares the outcome.
+      // S(i) done also means PV(i-2) done: P buffer sb is free again.
+      alive = named_and(1, 256, tid != 0 || wait_bar(&s_full[sb], (i >> 1) & 1, s_abort, p.flags));
       if (!alive) break;
       tc_fence_after();
-      uint32_t sv[N];
-#pragma unroll
-      for (int c = 0; c < N / 16; ++c)
-        tmem_ld16(tmem + lane_base + T::SCOL + N * b + 16 * c, sv + 16 * c);
-      tmem_wait_ld<N>(sv);
       const int tile_tok0 = u.tok_begin + i * kTileTok;
-      const int tok = tile_tok0 + tid;
+      const int tok = tile_tok0 + j;
       const bool tok_ok = tok < tok_end;
       const bool mask_rows = tile_tok0 + kTileTok - 1 > min_lim;
-      float t[N];
       bool trig = false;
+      if (active) {
 #pragma unroll
-      for (int r = 0; r < N; ++r) {
-        const float4 rp = s_rowp[r];
-        float x = fmaf(__uint_as_float(sv[r]), rp.x, rp.y);
-        if (!tok_ok || (mask_rows && tok > __float_as_int(rp.w))) x = -INFINITY;
-        trig |= x > rp.z;
-        t[r] = x;
+        for (int ch = 0; ch < NCH; ++ch) {
+          float x[CW];
+          scores(ch, sb, tok_ok, mask_rows, tok, x);
+          const float4* th = reinterpret_cast<const float4*>(s_thr + c0 + ch * CW);
+#pragma unroll
+          for (int e4 = 0; e4 < CW / 4; ++e4) {
+            const float4 t4 = th[e4];
+            trig |= (x[4 * e4] > t4.x) | (x[4 * e4 + 1] > t4.y) | (x[4 * e4 + 2] > t4.z) |
+                    (x[4 * e4 + 3] > t4.w);
+          }
+        }
       }
-      if (named_or(1, 128, trig)) {
+      if (named_or(1, 256, trig)) {
         // ---- raise the running maxima to the tile's exact row maxima ----
         if (tid < N) s_max[tid] = INT32_MIN;
-        named_sync(1, 128);
+        named_sync(1, 256);
+        if (active) {
 #pragma unroll
-        for (int r = 0; r < N; ++r) {
-          const int k = __reduce_max_sync(0xffffffffu, fkey(t[r]));
-          if (lane == 0) atomicMax(&s_max[r], k);
+          for (int ch = 0; ch < NCH; ++ch) {
+            float x[CW];
+            scores(ch, sb, tok_ok, mask_rows, tok, x);
+#pragma unroll
+            for (int e = 0; e < CW; ++e) {
+              const int k = __reduce_max_sync(0xffffffffu, fkey(x[e]));
+              if (lane == 0) atomicMax(&s_max[c0 + ch * CW + e], k);
+            }
+          }
         }
-        named_sync(1, 128);
+        named_sync(1, 256);
         bool moved = false;
         if (tid < N) {
           const int r = tid;
           const float tm = funkey(s_max[r]);  // tile max, relative to the old m_use
           const float m_old = s_m[r];
-          float delta = 0.f, corr = 1.f;
+          float corr = 1.f;
           if (tm != -INFINITY && (m_old == -INFINITY || tm > 0.f)) {
-            const float m_use_old = (m_old == -INFINITY) ? 0.f : m_old;
-            const float m_new = m_use_old + tm;
-            delta = tm;
+            const float m_new = (m_old == -INFINITY ? 0.f : m_old) + tm;
             if (m_old != -INFINITY) corr = ex2(m_old - m_new);
             s_m[r] = m_new;
-            float4 rp = s_rowp[r];
-            rp.y = -m_new;
-            rp.z = kRaise;
-            s_rowp[r] = rp;
+            s_nm[r] = -m_new;
+            s_thr[r] = kRaise;
             moved = corr != 1.f;
           }
-          s_delta[r] = delta;
           s_corr[r] = corr;
         }
-        const bool rescale = named_or(1, 128, moved) && i > 0;
+        const bool rescale = named_or(1, 256, moved) && i > 0;
 #pragma unroll
-        for (int r = 0; r < N; ++r) {
-          t[r] -= s_delta[r];
-          lpart[r] *= s_corr[r];
-        }
+        for (int r = 0; r < NH; ++r) lpart[r] *= s_corr[c0 + r];
         if (rescale) {  // O^T columns *= corr, once PV(i-1) is done
-          alive = named_and(1, 128,
-                            wait_bar(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, s_abort, p.flags));
+          alive = named_and(1, 256,
+                            tid != 0 || wait_bar(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1,
+                                                 s_abort, p.flags));
           if (!alive) break;
           tc_fence_after();
-          uint32_t ov[N];
+          if (active) {
 #pragma unroll
-          for (int c = 0; c < N / 16; ++c)
-            tmem_ld16(tmem + lane_base + T::OCOL + 16 * c, ov + 16 * c);
-          tmem_wait_ld<N>(ov);
+            for (int ch = 0; ch < NCH; ++ch) {
+              uint32_t ov[CW];
+              const uint32_t oa = tmem + lane_base + T::OCOL + c0 + ch * CW;
+              tmem_ld<CW>(oa, ov);
+              tmem_wait_ld<CW>(ov);
 #pragma unroll
-          for (int r = 0; r < N; ++r)
-            ov[r] = __float_as_uint(__uint_as_float(ov[r]) * s_corr[r]);
-#pragma unroll
-          for (int c = 0; c < N / 16; ++c)
-            tmem_st16(tmem + lane_base + T::OCOL + 16 * c, ov + 16 * c);
-          tmem_wait_st();
+              for (int e = 0; e < CW; ++e)
+                ov[e] = __float_as_uint(__uint_as_float(ov[e]) * s_corr[c0 + ch * CW + e]);
+              tmem_st<CW>(oa, ov);
+            }
+            tmem_wait_st();
+          }
         }
       }
-      // ---- p = 2^t, partial sums, P^T row of this token ----------------
-      uint8_t* prow = sP + b * T::PB;
+      // ---- p = 2^x, partial sums, P^T row segment of this token ----------
+      if (active) {
+        uint8_t* pt = sP + sb * T::PB;
 #pragma unroll
-      for (int c = 0; c < N / 8; ++c) {
-        uint32_t h[4];
+        for (int ch = 0; ch < NCH; ++ch) {
+          float x[CW];
+          scores(ch, sb, tok_ok, mask_rows, tok, x);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = ex2(t[8 * c + 2 * e]), p1 = ex2(t[8 * c + 2 * e + 1]);
-          lpart[8 * c + 2 * e] += p0;
-          lpart[8 * c + 2 * e + 1] += p1;
-          h[e] = f32x2_to_f16x2(p0, p1);
+          for (int c8 = 0; c8 < CW / 8; ++c8) {
+            uint32_t h[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int r0 = 8 * c8 + 2 * e;
+              const float p0 = ex2(x[r0]), p1 = ex2(x[r0 + 1]);
+              lpart[ch * CW + r0] += p0;
+              lpart[ch * CW + r0 + 1] += p1;
+              h[e] = f32x2_to_f16x2(p0, p1);
+            }
+            const uint32_t off = (uint32_t)(j >> 3) * (8 * T::ROWB) + (j & 7) * T::ROWB +
+                                 ((c0 + ch * CW) / 8 + c8) * 16;
+            *reinterpret_cast<uint4*>(pt + swz<T::PSWB>(off)) =
+                make_uint4(h[0], h[1], h[2], h[3]);
+          }
         }
-        const uint32_t off =
-            (uint32_t)(tid >> 3) * (8 * T::ROWB) + (tid & 7) * T::ROWB + c * 16;
-        *reinterpret_cast<uint4*>(prow + swz<T::PSWB>(off)) = make_uint4(h[0], h[1], h[2], h[3]);
       }
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[b]);
+      if (lane == 0) mbar_arrive(&p_full[sb]);
     }
 
-    // ---- epilogue: O^T row of value dim `tid`, all rows of the block ------
+    // ---- epilogue: O^T row of value dim j, this thread's row columns ------
     if (alive && ntiles > 0)
-      alive = named_and(1, 128,
-                        wait_bar(&pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, s_abort,
-                                 p.flags));
+      alive = named_and(1, 256,
+                        tid != 0 || wait_bar(&pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1,
+                                             s_abort, p.flags));
     if (alive) {
       tc_fence_after();
 #pragma unroll
-      for (int r = 0; r < N; ++r) {
+      for (int r = 0; r < NH; ++r) {
         float v = lpart[r];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) s_l[warp * N + r] = v;
+        if (lane == 0) s_l[q4 * N + c0 + r] = v;
       }
-      uint32_t ov[N];
-#pragma unroll
-      for (int c = 0; c < N / 16; ++c) tmem_ld16(tmem + lane_base + T::OCOL + 16 * c, ov + 16 * c);
-      tmem_wait_ld<N>(ov);
-      named_sync(1, 128);
+      named_sync(1, 256);
       constexpr float kLn2 = 0.69314718055994530942f;
       const bool partial = p.split && u.num_splits > 1;
       const int Hq = p.num_qo_heads;
+      if (active) {
 #pragma unroll
-      for (int r = 0; r < N; ++r) {
-        const int gr = row0 + r;
-        if (gr >= R) break;
-        const float L = s_l[r] + s_l[N + r] + s_l[2 * N + r] + s_l[3 * N + r];
-        const float m = s_m[r];
-        const bool any = L > 0.f && m != -INFINITY;
-        const float o = any ? __uint_as_float(ov[r]) * (p.v_scale / L) : 0.f;
-        const float lse_v = any ? (m + log2f(L)) * kLn2 : -INFINITY;
-        const int qi = gr / G, head = u.h_kv * G + gr % G;
-        const int64_t qrow = u.qo_begin + qi;
-        if (!partial) {
-          p.out[(qrow * Hq + head) * DV + tid] = f32_to_bf16_bits(o);
-          if (tid == 0 && p.lse) p.lse[qrow * Hq + head] = lse_v;
-        } else {
-          const int64_t pi = (int64_t)u.partial_base +
-                             ((int64_t)qi * Hq + head) * u.num_splits + u.split;
-          p.partial_o[pi * DV + tid] = o;
-          if (tid == 0) p.partial_lse[pi] = lse_v;
+        for (int ch = 0; ch < NCH; ++ch) {
+          uint32_t ov[CW];
+          tmem_ld<CW>(tmem + lane_base + T::OCOL + c0 + ch * CW, ov);
+          tmem_wait_ld<CW>(ov);
+#pragma unroll
+          for (int e = 0; e < CW; ++e) {
+            const int col = c0 + ch * CW + e, gr = row0 + col;
+            if (col < nvalid) {
+              const float L = s_l[col] + s_l[N + col] + s_l[2 * N + col] + s_l[3 * N + col];
+              const float m = s_m[col];
+              const bool any = L > 0.f && m != -INFINITY;
+              const float o = any ? __uint_as_float(ov[e]) * (p.v_scale / L) : 0.f;
+              const float lse_v = any ? (m + log2f(L)) * kLn2 : -INFINITY;
+              const int qi = gr / G, head = u.h_kv * G + gr % G;
+              const int64_t qrow = u.qo_begin + qi;
+              if (!partial) {
+                p.out[(qrow * Hq + head) * DV + j] = f32_to_bf16_bits(o);
+                if (j == 0 && p.lse) p.lse[qrow * Hq + head] = lse_v;
+              } else {
+                const int64_t pi = (int64_t)u.partial_base +
+                                   ((int64_t)qi * Hq + head) * u.num_splits + u.split;
+                p.partial_o[pi * DV + j] = o;
+                if (j == 0) p.partial_lse[pi] = lse_v;
+              }
+            }
+          }
         }
       }
       if (partial)
-        merge_if_last<N, DV, 128>(p, u, row0, R, s_fin, tid, [] { named_sync(1, 128); });
+        merge_if_last<N, DV, 256>(p, u, row0, R, s_fin, tid, [] { named_sync(1, 256); });
     }
     tc_fence_before();
   }
 
   // ---- every role is done: release tensor memory -------------------------
   __syncthreads();
-  if (warp == 8) {
+  if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, T::TCOLS);
   }
