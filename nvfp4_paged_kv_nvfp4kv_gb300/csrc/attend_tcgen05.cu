@@ -22,14 +22,14 @@
 //    128-byte-swizzled operand layout.  Three K_hat / V_hat buffers.
 //  * softmax (warps 0-7; thread = token for S^T, = value dim for O^T, one
 //    half of the query-row columns): tcgen05.ld of its S^T row, p = 2^(x - m)
-//    written as the f16 P^T operand, per-row partial sums kept per thread and
-//    added up once at the end.
+//    written as the f16 P^T operand.
 //  * product issue (warp 16, one thread): S^T = K_hat . Q^T (M = 128 tokens,
 //    N rows, K = Dk; A from tensor memory, B = Q in shared memory) into one
 //    of two tensor-memory tiles, and O^T += V_hat^T . P^T (M = 128 value
 //    dims, N rows, K = 128 tokens; both operands MN-major in shared memory)
-//    accumulated in tensor memory over the unit, each as soon as its inputs
-//    are ready; tcgen05.commit signals them on mbarriers.  One thread can
+//    accumulated in tensor memory over the unit, with the row sums
+//    l += 1^T . P^T beside it (A = a block of ones in tensor memory), each as
+//    soon as its inputs are ready; tcgen05.commit signals them on mbarriers.  One thread can
 //    issue a product about every 54 cycles, whatever N, so this layout suits
 //    many query rows per kv head (extend); decode keeps the mma.sync kernel.
 // Putting the tile's tokens on the M side fills the 128-row MMA even for a
@@ -290,14 +290,17 @@ struct Tg5 {
   static constexpr int OFF_MISC = OFF_RAW + RS * STAGE;
   static constexpr int MISC = 8192;
   static constexpr int SMEM = OFF_MISC + MISC + 1024;  // + alignment slack
-  // tensor memory columns: K_hat x3 (64 each), S^T x2 (N each), O^T (N)
-  static constexpr int KCOL = 0, SCOL = 64 * kKB, OCOL = SCOL + 2 * N;
-  static constexpr int TCOLS = (OCOL + N) <= 256 ? 256 : 512;
+  // tensor memory columns: K_hat x3 (64 each), S^T x2 (N each), O^T (N),
+  // row sums (N; every lane holds them), a 128 x 16 block of f16 ones (8)
+  static constexpr int KCOL = 0, SCOL = 64 * kKB, OCOL = SCOL + 2 * N, LCOL = OCOL + N;
+  static constexpr int ONES = LCOL + N;
+  static constexpr int TCOLS = (ONES + 8) <= 256 ? 256 : 512;
   static constexpr uint32_t IDESC_QK = idesc_f16(128, N, 0, 0);
   static constexpr uint32_t IDESC_PV = idesc_f16(128, N, 1, 1);
+  static constexpr uint32_t IDESC_L = idesc_f16(128, N, 0, 1);
   static_assert(OFF_P % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_RAW % 1024 == 0, "align");
   static_assert(STAGE % 1024 == 0 && OFF_MISC % 16 == 0, "align");
-  static_assert(OCOL + N <= TCOLS, "tensor memory");
+  static_assert(ONES + 8 <= TCOLS, "tensor memory");
   static_assert(SMEM <= 232448, "shared memory");
 };
 
@@ -338,11 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
   float* s_thr = s_nm + N;
   int* s_lim = reinterpret_cast<int*>(s_thr + N);
   float* s_m = reinterpret_cast<float*>(s_lim + N);     // running max (log2)
-  int* s_max = reinterpret_cast<int*>(s_m + N);         // reduction keys
+  int* s_max = reinterpret_cast<int*>(s_m + N);         // reduction keys, then shifts
   float* s_corr = reinterpret_cast<float*>(s_max + N);
   int* s_qamax = reinterpret_cast<int*>(s_corr + N);
-  float* s_l = reinterpret_cast<float*>(s_qamax + N);   // [4][N]
-  float* s_fin = s_l + 4 * N;                           // [2N + 1]
+  float* s_fin = reinterpret_cast<float*>(s_qamax + N);  // [2N + 1]
 
   const WorkUnit u = p.units[blockIdx.x];
   const int G = p.group;
@@ -506,11 +508,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
         tc_fence_after();
         const int bi = i % kKB, sb = i & 1;
         const uint64_t vd = vd0 + ((bi * T::VH) >> 4), pd = pd0 + ((sb * T::PB) >> 4);
-        umma_ss(tmem + T::OCOL, vd, pd, T::IDESC_PV, i > 0 ? 1u : 0u);
+        // O^T += V_hat^T P^T and the row sums l += 1^T P^T (A = ones)
 #pragma unroll
-        for (int k = 1; k < kTileTok / 16; ++k)
-          umma_ss(tmem + T::OCOL, vd + ((k * 2048) >> 4), pd + ((k * 16 * T::ROWB) >> 4),
-                  T::IDESC_PV, 1u);
+        for (int k = 0; k < kTileTok / 16; ++k) {
+          const uint64_t pk = pd + ((k * 16 * T::ROWB) >> 4);
+          const uint32_t acc = (i > 0 || k > 0) ? 1u : 0u;
+          umma_ss(tmem + T::OCOL, vd + ((k * 2048) >> 4), pk, T::IDESC_PV, acc);
+          umma_ts(tmem + T::LCOL, tmem + T::ONES, pk, T::IDESC_L, acc);
+        }
         umma_commit(&pv_done[sb]);
         umma_commit(&kv_empty[bi]);
       };
@@ -610,7 +615,15 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
       }
       s_m[r] = -INFINITY;
     }
+    if (warp < 4) {  // the ones block of the row-sum product, lanes 32 warp ..
+      uint32_t ones[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ones[e] = 0x3C003C00u;  // f16 1.0 pairs
+      tmem_st8(tmem + lane_base + T::ONES, ones);
+      tmem_wait_st();
+    }
     fence_async_smem();
+    tc_fence_before();
     named_sync(1, 256);
     __syncwarp();
     if (lane == 0) mbar_arrive(q_full);
@@ -642,9 +655,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
       }
     };
 
-    float lpart[NH];
-#pragma unroll
-    for (int r = 0; r < NH; ++r) lpart[r] = 0.f;
     bool alive = true;
     for (int i = 0; i < ntiles; ++i) {
       const int sb = i & 1;
@@ -657,19 +667,22 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
       const int tok = tile_tok0 + j;
       const bool tok_ok = tok < tok_end;
       const bool mask_rows = tile_tok0 + kTileTok - 1 > min_lim;
+      float x[NH];
       bool trig = false;
       if (active) {
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
-          float x[CW];
-          scores(ch, sb, tok_ok, mask_rows, tok, x);
+          float xc[CW];
+          scores(ch, sb, tok_ok, mask_rows, tok, xc);
           const float4* th = reinterpret_cast<const float4*>(s_thr + c0 + ch * CW);
 #pragma unroll
           for (int e4 = 0; e4 < CW / 4; ++e4) {
             const float4 t4 = th[e4];
-            trig |= (x[4 * e4] > t4.x) | (x[4 * e4 + 1] > t4.y) | (x[4 * e4 + 2] > t4.z) |
-                    (x[4 * e4 + 3] > t4.w);
+            trig |= (xc[4 * e4] > t4.x) | (xc[4 * e4 + 1] > t4.y) | (xc[4 * e4 + 2] > t4.z) |
+                    (xc[4 * e4 + 3] > t4.w);
           }
+#pragma unroll
+          for (int e = 0; e < CW; ++e) x[ch * CW + e] = xc[e];
         }
       }
       if (named_or(1, 256, trig)) {
@@ -678,14 +691,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
         named_sync(1, 256);
         if (active) {
 #pragma unroll
-          for (int ch = 0; ch < NCH; ++ch) {
-            float x[CW];
-            scores(ch, sb, tok_ok, mask_rows, tok, x);
-#pragma unroll
-            for (int e = 0; e < CW; ++e) {
-              const int k = __reduce_max_sync(0xffffffffu, fkey(x[e]));
-              if (lane == 0) atomicMax(&s_max[c0 + ch * CW + e], k);
-            }
+          for (int e = 0; e < NH; ++e) {
+            const int k = __reduce_max_sync(0xffffffffu, fkey(x[e]));
+            if (lane == 0) atomicMax(&s_max[c0 + e], k);
           }
         }
         named_sync(1, 256);
@@ -694,21 +702,23 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
           const int r = tid;
           const float tm = funkey(s_max[r]);  // tile max, relative to the old m_use
           const float m_old = s_m[r];
-          float corr = 1.f;
+          float corr = 1.f, delta = 0.f;
           if (tm != -INFINITY && (m_old == -INFINITY || tm > 0.f)) {
             const float m_new = (m_old == -INFINITY ? 0.f : m_old) + tm;
             if (m_old != -INFINITY) corr = ex2(m_old - m_new);
+            delta = tm;
             s_m[r] = m_new;
             s_nm[r] = -m_new;
             s_thr[r] = kRaise;
             moved = corr != 1.f;
           }
           s_corr[r] = corr;
+          s_max[r] = __float_as_int(delta);
         }
         const bool rescale = named_or(1, 256, moved) && i > 0;
 #pragma unroll
-        for (int r = 0; r < NH; ++r) lpart[r] *= s_corr[c0 + r];
-        if (rescale) {  // O^T columns *= corr, once PV(i-1) is done
+        for (int e = 0; e < NH; ++e) x[e] -= __int_as_float(s_max[c0 + e]);
+        if (rescale) {  // O^T and row-sum columns *= corr, once PV(i-1) is done
           alive = named_and(1, 256,
                             tid != 0 || wait_bar(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1,
                                                  s_abort, p.flags));
@@ -716,43 +726,35 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
           tc_fence_after();
           if (active) {
 #pragma unroll
-            for (int ch = 0; ch < NCH; ++ch) {
-              uint32_t ov[CW];
-              const uint32_t oa = tmem + lane_base + T::OCOL + c0 + ch * CW;
-              tmem_ld<CW>(oa, ov);
-              tmem_wait_ld<CW>(ov);
+            for (int blk = 0; blk < 2; ++blk)
 #pragma unroll
-              for (int e = 0; e < CW; ++e)
-                ov[e] = __float_as_uint(__uint_as_float(ov[e]) * s_corr[c0 + ch * CW + e]);
-              tmem_st<CW>(oa, ov);
-            }
+              for (int ch = 0; ch < NCH; ++ch) {
+                uint32_t ov[CW];
+                const uint32_t oa =
+                    tmem + lane_base + (blk ? T::LCOL : T::OCOL) + c0 + ch * CW;
+                tmem_ld<CW>(oa, ov);
+                tmem_wait_ld<CW>(ov);
+#pragma unroll
+                for (int e = 0; e < CW; ++e)
+                  ov[e] = __float_as_uint(__uint_as_float(ov[e]) * s_corr[c0 + ch * CW + e]);
+                tmem_st<CW>(oa, ov);
+              }
             tmem_wait_st();
           }
         }
       }
-      // ---- p = 2^x, partial sums, P^T row segment of this token ----------
+      // ---- p = 2^x: the P^T row segment of this token --------------------
       if (active) {
         uint8_t* pt = sP + sb * T::PB;
 #pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) {
-          float x[CW];
-          scores(ch, sb, tok_ok, mask_rows, tok, x);
+        for (int c8 = 0; c8 < NH / 8; ++c8) {
+          uint32_t h[4];
 #pragma unroll
-          for (int c8 = 0; c8 < CW / 8; ++c8) {
-            uint32_t h[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int r0 = 8 * c8 + 2 * e;
-              const float p0 = ex2(x[r0]), p1 = ex2(x[r0 + 1]);
-              lpart[ch * CW + r0] += p0;
-              lpart[ch * CW + r0 + 1] += p1;
-              h[e] = f32x2_to_f16x2(p0, p1);
-            }
-            const uint32_t off = (uint32_t)(j >> 3) * (8 * T::ROWB) + (j & 7) * T::ROWB +
-                                 ((c0 + ch * CW) / 8 + c8) * 16;
-            *reinterpret_cast<uint4*>(pt + swz<T::PSWB>(off)) =
-                make_uint4(h[0], h[1], h[2], h[3]);
-          }
+          for (int e = 0; e < 4; ++e)
+            h[e] = f32x2_to_f16x2(ex2(x[8 * c8 + 2 * e]), ex2(x[8 * c8 + 2 * e + 1]));
+          const uint32_t off =
+              (uint32_t)(j >> 3) * (8 * T::ROWB) + (j & 7) * T::ROWB + (c0 / 8 + c8) * 16;
+          *reinterpret_cast<uint4*>(pt + swz<T::PSWB>(off)) = make_uint4(h[0], h[1], h[2], h[3]);
         }
       }
       fence_async_smem();
@@ -768,28 +770,22 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
                                              s_abort, p.flags));
     if (alive) {
       tc_fence_after();
-#pragma unroll
-      for (int r = 0; r < NH; ++r) {
-        float v = lpart[r];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) s_l[q4 * N + c0 + r] = v;
-      }
-      named_sync(1, 256);
       constexpr float kLn2 = 0.69314718055994530942f;
       const bool partial = p.split && u.num_splits > 1;
       const int Hq = p.num_qo_heads;
       if (active) {
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
-          uint32_t ov[CW];
+          uint32_t ov[CW], lv[CW];
           tmem_ld<CW>(tmem + lane_base + T::OCOL + c0 + ch * CW, ov);
+          tmem_ld<CW>(tmem + lane_base + T::LCOL + c0 + ch * CW, lv);
           tmem_wait_ld<CW>(ov);
+          tmem_wait_ld<CW>(lv);
 #pragma unroll
           for (int e = 0; e < CW; ++e) {
             const int col = c0 + ch * CW + e, gr = row0 + col;
             if (col < nvalid) {
-              const float L = s_l[col] + s_l[N + col] + s_l[2 * N + col] + s_l[3 * N + col];
+              const float L = __uint_as_float(lv[e]);
               const float m = s_m[col];
               const bool any = L > 0.f && m != -INFINITY;
               const float o = any ? __uint_as_float(ov[e]) * (p.v_scale / L) : 0.f;
