@@ -139,7 +139,9 @@ typedef struct nvfp4kv_plan_options {
   int32_t disable_split;      /* nonzero: one work unit per (request, head)  */
   int32_t max_splits;         /* >0: at most this many chunks per request    */
   int32_t force_chunk_tokens; /* >0: chunk size in tokens, multiple of 16    */
-  int32_t kernel;             /* 0 auto, 1 tensor-core (mma.sync), 2 CUDA-core,
+  int32_t kernel;             /* 0 auto (3 when head dims are 128 and a kv
+                                 head has more than 16 query rows, else 1),
+                                 1 tensor-core (mma.sync), 2 CUDA-core,
                                  3 tcgen05 (head dims 128 x 128 only)      */
   int32_t num_sms;            /* >0: override the device's SM count          */
   int32_t ctas_per_sm;        /* >0: override the occupancy query            */

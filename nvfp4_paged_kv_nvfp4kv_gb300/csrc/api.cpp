@@ -298,7 +298,13 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
   // ---- kernel choice and occupancy --------------------------------------
   int kind = opts.kernel;
   AttendConfig cfg{};
-  if (kind == 0) kind = kKernelTensorCore;
+  // auto: the tcgen05 kernel where a kv head has many query rows (extend):
+  // it dequantises each page once for all of them and its products grow
+  // with the rows; for a few rows (decode) the mma.sync register path is
+  // cheaper (a tcgen05 product costs ~54 cycles to issue whatever its N)
+  if (kind == 0)
+    kind = (head_dim_qk == 128 && head_dim_vo == 128 && max_rows > 16) ? kKernelTcgen05
+                                                                       : kKernelTensorCore;
   // occupancy is sized on the bulk-copy variant (the contiguous-page path)
   const int want_rows = kind == kKernelTcgen05 ? std::max(max_rows, 1) : (max_rows <= 8 ? 8 : 16);
   if (!lookup_kernel(kind, head_dim_qk, head_dim_vo, want_rows, true, &cfg))

@@ -271,3 +271,18 @@ def test_plan_tcgen05_rejects_other_dims():
                                            kv_lens=(100,)))
     with pytest.raises(N.NvFp4KvError):
         plan(batch, kernel=3)
+
+
+def test_plan_auto_kernel_choice():
+    """Auto picks tcgen05 for many query rows per kv head at head dims 128
+    (extend) and the mma.sync kernel for decode or other head dims."""
+    ext = W.make_batch(W.custom_workload(batch=2, qo_len=16, num_qo_heads=8, num_kv_heads=2,
+                                         kv_lens=(100, 900), causal=True))
+    assert plan(ext, ctas_per_sm=1).info.kernel == 3
+    dec = W.make_batch(W.custom_workload(batch=2, qo_len=1, num_qo_heads=8, num_kv_heads=2,
+                                         kv_lens=(100, 900)))
+    assert plan(dec).info.kernel == 1
+    wide = W.make_batch(W.custom_workload(batch=2, qo_len=16, num_qo_heads=8, num_kv_heads=2,
+                                          head_dim_qk=256, head_dim_vo=256,
+                                          kv_lens=(100, 900), causal=True))
+    assert plan(wide).info.kernel == 1
