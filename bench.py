@@ -38,7 +38,8 @@ UNIT = "KV tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attend_tc_long_context_decode.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "nvfp4_paged_kv_nvfp4kv_gb300", "csrc", f)
-                  for f in ("attend_tc.cu", "device_common.cuh", "internal.h")]
+                  for f in ("attend_tc.cu", "append_fused.cuh", "device_common.cuh",
+                            "epilogue.cuh", "internal.h", "quantize.cuh", "stage.cuh")]
 
 
 def workload_desc(cfg: W.Workload) -> str:
