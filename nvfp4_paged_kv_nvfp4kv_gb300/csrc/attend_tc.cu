@@ -87,6 +87,10 @@ constexpr int tc_min_blocks() {
   return (DK <= 128 && DV <= 128 && NT == 1) ? NVFP4KV_TC_MINB : 1;
 }
 
+// One row block: the running maximum is raised only when a score exceeds it
+// by more than this (log2 domain), so p <= 2^kRaiseLog2 fits f16.
+constexpr float kRaiseLog2 = 8.f;
+
 // Polls of a stage's barrier before the kernel gives up on a bulk copy.
 constexpr uint32_t kWaitLimit = 1u << 20;
 
@@ -254,6 +258,20 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
   }
   for (int rr = 0; rr < T::RB; ++rr)
     if (sRowLim[rr] >= 0) min_lim = min(min_lim, sRowLim[rr]);
+  // one row block (NT == 1): this lane's query rows 2t and 2t+1, score
+  // factor f, -m_use, raise threshold (-inf until the row has a maximum,
+  // +inf for padding rows), causal limit, running max and partial sum
+  float f2[2], nm2[2], thr2[2], mrow[2], lrow[2];
+  int lim2[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    f2[k] = sRowF[(2 * t + k) % T::RB];
+    lim2[k] = sRowLim[(2 * t + k) % T::RB];
+    nm2[k] = 0.f;
+    thr2[k] = lim2[k] >= 0 ? -INFINITY : INFINITY;
+    mrow[k] = -INFINITY;
+    lrow[k] = 0.f;
+  }
 
   // Q fragments: k-step kk of chunk c = kk / KS_PER_CH, step m within it,
   // covers the 4 consecutive dims starting at 2*(4c+t)*CB + 4m.
@@ -316,116 +334,229 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
     const uint8_t* st = wpipe + (i % STAGES) * T::STAGE_BYTES;
     const int tok0 = u.tok_begin + (warp + i * WARPS) * 16;
 
-    // ---- S = Q K^T for tokens tok0 .. tok0+15 (two n-tiles) -------------
-    // two accumulators per n-tile (alternate k-steps) halve the dependent
-    // mma chain; they are added after the last k-step
-    float sacc[2][4], sacc2[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        sacc[nt][k] = 0.f;
-        sacc2[nt][k] = 0.f;
+    uint32_t pfrag[NT][2];
+    // K row `row` (a token of the page), 16-byte chunk ch of this lane
+    auto krow = [&](int row, int ch, uint32_t (&w)[T::CB / 4], uint32_t& sc0, uint32_t& sc1) {
+      if constexpr (T::CB == 16) {
+        const int pos = T::S::k_pos(row, ch);
+        const uint4 v = *reinterpret_cast<const uint4*>(st + row * T::KROW + pos * 16);
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+        const uint32_t sfp = *reinterpret_cast<const uint16_t*>(
+            st + T::OFF_KSF + row * T::KSFROW + 2 * ch);
+        const uint32_t s2 = e4m3x2_to_f16x2(sfp);
+        sc0 = bcast_lo(s2);
+        sc1 = bcast_hi(s2);
+      } else {
+        const uint2 v = *reinterpret_cast<const uint2*>(st + row * T::KROW + ch * 8);
+        w[0] = v.x; w[1] = v.y;
+        const uint32_t sfb = st[T::OFF_KSF + row * T::KSFROW + ch];
+        sc0 = bcast_lo(e4m3x2_to_f16x2(sfb));
+        sc1 = sc0;
       }
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const int row = 8 * nt + g;
+    };
+    if constexpr (NT == 1) {
+      // ---- S^T = K_hat Q^T: tokens g, g+8 (M = 16) x query rows (N = 8) --
+      // A = K_hat (the two token rows this lane reads), B = the Q rows'
+      // fragments; two accumulators (alternate k-steps) halve the chain
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < T::NCH; ++c) {
         const int ch = 4 * c + t;
-        uint32_t w[T::CB / 4];
-        uint32_t sc0, sc1;
-        if constexpr (T::CB == 16) {
-          const int pos = T::S::k_pos(row, ch);
-          const uint4 v = *reinterpret_cast<const uint4*>(st + row * T::KROW + pos * 16);
-          w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-          const uint32_t sfp = *reinterpret_cast<const uint16_t*>(
-              st + T::OFF_KSF + row * T::KSFROW + 2 * ch);
-          const uint32_t s2 = e4m3x2_to_f16x2(sfp);
-          sc0 = bcast_lo(s2);
-          sc1 = bcast_hi(s2);
-        } else {
-          const uint2 v = *reinterpret_cast<const uint2*>(st + row * T::KROW + ch * 8);
-          w[0] = v.x; w[1] = v.y;
-          const uint32_t sfb = st[T::OFF_KSF + row * T::KSFROW + ch];
-          sc0 = bcast_lo(e4m3x2_to_f16x2(sfb));
-          sc1 = sc0;
-        }
+        uint32_t wg[T::CB / 4], w8[T::CB / 4], sg0, sg1, s80, s81;
+        krow(g, ch, wg, sg0, sg1);
+        krow(8 + g, ch, w8, s80, s81);
 #pragma unroll
         for (int q = 0; q < T::CB / 4; ++q) {
-          uint32_t h[4];
-          e2m1x8_to_f16x8(w[q], h);
-          const uint32_t sc = (T::CB == 16 && q >= 2) ? sc1 : sc0;
+          uint32_t hg[4], h8[4];
+          e2m1x8_to_f16x8(wg[q], hg);
+          e2m1x8_to_f16x8(w8[q], h8);
+          const bool hi = T::CB == 16 && q >= 2;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) h[j] = hmul2(h[j], sc);
+          for (int j = 0; j < 4; ++j) {
+            hg[j] = hmul2(hg[j], hi ? sg1 : sg0);
+            h8[j] = hmul2(h8[j], hi ? s81 : s80);
+          }
           const int kk = c * T::KS_PER_CH + 2 * q;
-          uint32_t a0[4], a1[4];
+          uint32_t b0[4], b1[4];
           if constexpr (T::Q_IN_REGS) {
 #pragma unroll
             for (int x = 0; x < 4; ++x) {
-              a0[x] = qreg[kk][x];
-              a1[x] = qreg[kk + 1][x];
+              b0[x] = qreg[kk][x];
+              b1[x] = qreg[kk + 1][x];
             }
           } else {
-            q_frag(kk, a0);
-            q_frag(kk + 1, a1);
+            q_frag(kk, b0);
+            q_frag(kk + 1, b1);
           }
-          mma_16816(sacc[nt], a0, h[0], h[1]);
-          mma_16816(sacc2[nt], a1, h[2], h[3]);
+          const uint32_t a0[4] = {hg[0], h8[0], hg[1], h8[1]};
+          const uint32_t a1[4] = {hg[2], h8[2], hg[3], h8[3]};
+          mma_16816(sa, a0, b0[0], b0[2]);
+          mma_16816(sb, a1, b1[0], b1[2]);
         }
       }
-    }
+      // ---- softmax with a lazily raised maximum (log2 domain) -----------
+      // x[0..3] = tokens g, g, g+8, g+8 x rows 2t, 2t+1, 2t, 2t+1
+      float x[4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+      for (int k = 0; k < 4; ++k) x[k] = fmaf(sa[k] + sb[k], f2[k & 1], nm2[k & 1]);
+      if (tok0 + 15 > min_lim) {
+        const int ta = tok0 + g, tb = tok0 + g + 8;
+        if (ta > lim2[0]) x[0] = -INFINITY;
+        if (ta > lim2[1]) x[1] = -INFINITY;
+        if (tb > lim2[0]) x[2] = -INFINITY;
+        if (tb > lim2[1]) x[3] = -INFINITY;
+      }
+      const bool trig = (x[0] > thr2[0]) | (x[2] > thr2[0]) | (x[1] > thr2[1]) | (x[3] > thr2[1]);
+      if (__any_sync(0xffffffffu, trig)) {
+        // raise each row's maximum to this page's exact maximum (a row's
+        // values sit in the 8 lanes of the same t)
+        float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
 #pragma unroll
-      for (int k = 0; k < 4; ++k) sacc[nt][k] += sacc2[nt][k];
+        for (int o = 4; o < 32; o <<= 1) {
+          mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], o));
+          mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], o));
+        }
+        float corr[2] = {1.f, 1.f};
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          if (mx[k] != -INFINITY && (mrow[k] == -INFINITY || mx[k] > 0.f)) {
+            if (mrow[k] != -INFINITY) corr[k] = ex2(-mx[k]);  // 2^(m_old - m_new)
+            mrow[k] = (mrow[k] == -INFINITY ? 0.f : mrow[k]) + mx[k];
+            nm2[k] = -mrow[k];
+            thr2[k] = kRaiseLog2;
+            x[k] -= mx[k];
+            x[k + 2] -= mx[k];
+          }
+          lrow[k] *= corr[k];
+        }
+        if (corr[0] != 1.f || corr[1] != 1.f) {
+#pragma unroll
+          for (int mt = 0; mt < T::MT; ++mt) {
+            oacc[mt][0][0] *= corr[0];
+            oacc[mt][0][1] *= corr[1];
+            oacc[mt][0][2] *= corr[0];
+            oacc[mt][0][3] *= corr[1];
+          }
+        }
+      }
+      const float p0 = ex2(x[0]), p1 = ex2(x[1]), p2 = ex2(x[2]), p3 = ex2(x[3]);
+      lrow[0] += p0 + p2;
+      lrow[1] += p1 + p3;
+      // P^T fragments for the PV product: transpose the two 8 x 8 blocks
+      // (tokens 0-7 and 8-15 x the 8 rows)
+      pfrag[0][0] = movmatrix_trans(f32x2_to_f16x2(p0, p1));
+      pfrag[0][1] = movmatrix_trans(f32x2_to_f16x2(p2, p3));
+    } else {
+      // ---- S = Q K^T for tokens tok0 .. tok0+15 (two n-tiles) -------------
+      // two accumulators per n-tile (alternate k-steps) halve the dependent
+      // mma chain; they are added after the last k-step
+      float sacc[2][4], sacc2[2][4];
+  #pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+  #pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          sacc[nt][k] = 0.f;
+          sacc2[nt][k] = 0.f;
+        }
+  #pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int row = 8 * nt + g;
+  #pragma unroll
+        for (int c = 0; c < T::NCH; ++c) {
+          const int ch = 4 * c + t;
+          uint32_t w[T::CB / 4];
+          uint32_t sc0, sc1;
+          if constexpr (T::CB == 16) {
+            const int pos = T::S::k_pos(row, ch);
+            const uint4 v = *reinterpret_cast<const uint4*>(st + row * T::KROW + pos * 16);
+            w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+            const uint32_t sfp = *reinterpret_cast<const uint16_t*>(
+                st + T::OFF_KSF + row * T::KSFROW + 2 * ch);
+            const uint32_t s2 = e4m3x2_to_f16x2(sfp);
+            sc0 = bcast_lo(s2);
+            sc1 = bcast_hi(s2);
+          } else {
+            const uint2 v = *reinterpret_cast<const uint2*>(st + row * T::KROW + ch * 8);
+            w[0] = v.x; w[1] = v.y;
+            const uint32_t sfb = st[T::OFF_KSF + row * T::KSFROW + ch];
+            sc0 = bcast_lo(e4m3x2_to_f16x2(sfb));
+            sc1 = sc0;
+          }
+  #pragma unroll
+          for (int q = 0; q < T::CB / 4; ++q) {
+            uint32_t h[4];
+            e2m1x8_to_f16x8(w[q], h);
+            const uint32_t sc = (T::CB == 16 && q >= 2) ? sc1 : sc0;
+  #pragma unroll
+            for (int j = 0; j < 4; ++j) h[j] = hmul2(h[j], sc);
+            const int kk = c * T::KS_PER_CH + 2 * q;
+            uint32_t a0[4], a1[4];
+            if constexpr (T::Q_IN_REGS) {
+  #pragma unroll
+              for (int x = 0; x < 4; ++x) {
+                a0[x] = qreg[kk][x];
+                a1[x] = qreg[kk + 1][x];
+              }
+            } else {
+              q_frag(kk, a0);
+              q_frag(kk + 1, a1);
+            }
+            mma_16816(sacc[nt], a0, h[0], h[1]);
+            mma_16816(sacc2[nt], a1, h[2], h[3]);
+          }
+        }
+      }
+  #pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+  #pragma unroll
+        for (int k = 0; k < 4; ++k) sacc[nt][k] += sacc2[nt][k];
 
-    // ---- online softmax (log2 domain), rows g and g+8 -------------------
-    const bool need_mask = tok0 + 15 > min_lim;
-    uint32_t pfrag[NT][2];
-    float corr[NT];
-#pragma unroll
-    for (int hf = 0; hf < NT; ++hf) {
-      float x[4] = {sacc[0][2 * hf] * rowf[hf], sacc[0][2 * hf + 1] * rowf[hf],
-                    sacc[1][2 * hf] * rowf[hf], sacc[1][2 * hf + 1] * rowf[hf]};
-      if (need_mask) {
-        const int j0 = tok0 + 2 * t;
-        if (j0 > rowlim[hf]) x[0] = -INFINITY;
-        if (j0 + 1 > rowlim[hf]) x[1] = -INFINITY;
-        if (j0 + 8 > rowlim[hf]) x[2] = -INFINITY;
-        if (j0 + 9 > rowlim[hf]) x[3] = -INFINITY;
+      // ---- online softmax (log2 domain), rows g and g+8 -------------------
+      const bool need_mask = tok0 + 15 > min_lim;
+      float corr[NT];
+  #pragma unroll
+      for (int hf = 0; hf < NT; ++hf) {
+        float x[4] = {sacc[0][2 * hf] * rowf[hf], sacc[0][2 * hf + 1] * rowf[hf],
+                      sacc[1][2 * hf] * rowf[hf], sacc[1][2 * hf + 1] * rowf[hf]};
+        if (need_mask) {
+          const int j0 = tok0 + 2 * t;
+          if (j0 > rowlim[hf]) x[0] = -INFINITY;
+          if (j0 + 1 > rowlim[hf]) x[1] = -INFINITY;
+          if (j0 + 8 > rowlim[hf]) x[2] = -INFINITY;
+          if (j0 + 9 > rowlim[hf]) x[3] = -INFINITY;
+        }
+        float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run[hf], mx);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        corr[hf] = ex2(m_run[hf] - m_use);
+        m_run[hf] = m_new;
+        const float p0 = ex2(x[0] - m_use), p1 = ex2(x[1] - m_use);
+        const float p2 = ex2(x[2] - m_use), p3 = ex2(x[3] - m_use);
+        l_run[hf] = l_run[hf] * corr[hf] + ((p0 + p1) + (p2 + p3));
+        pfrag[hf][0] = f32x2_to_f16x2(p0, p1);
+        pfrag[hf][1] = f32x2_to_f16x2(p2, p3);
       }
-      float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_new = fmaxf(m_run[hf], mx);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      corr[hf] = ex2(m_run[hf] - m_use);
-      m_run[hf] = m_new;
-      const float p0 = ex2(x[0] - m_use), p1 = ex2(x[1] - m_use);
-      const float p2 = ex2(x[2] - m_use), p3 = ex2(x[3] - m_use);
-      l_run[hf] = l_run[hf] * corr[hf] + ((p0 + p1) + (p2 + p3));
-      pfrag[hf][0] = f32x2_to_f16x2(p0, p1);
-      pfrag[hf][1] = f32x2_to_f16x2(p2, p3);
-    }
-    // rescale O^T columns (query rows 8nq+2t, 8nq+2t+1); skipped when no
-    // row maximum of the warp moved (corr == 1 exactly for every row)
-    bool moved = false;
-#pragma unroll
-    for (int hf = 0; hf < NT; ++hf) moved |= corr[hf] != 1.f;
-    if (__any_sync(0xffffffffu, moved)) {
-#pragma unroll
-    for (int nq = 0; nq < NT; ++nq) {
-      const float cA = __shfl_sync(0xffffffffu, corr[nq], (2 * t) * 4);
-      const float cB = __shfl_sync(0xffffffffu, corr[nq], (2 * t + 1) * 4);
-#pragma unroll
-      for (int mt = 0; mt < T::MT; ++mt) {
-        oacc[mt][nq][0] *= cA;
-        oacc[mt][nq][1] *= cB;
-        oacc[mt][nq][2] *= cA;
-        oacc[mt][nq][3] *= cB;
+      // rescale O^T columns (query rows 8nq+2t, 8nq+2t+1); skipped when no
+      // row maximum of the warp moved (corr == 1 exactly for every row)
+      bool moved = false;
+  #pragma unroll
+      for (int hf = 0; hf < NT; ++hf) moved |= corr[hf] != 1.f;
+      if (__any_sync(0xffffffffu, moved)) {
+  #pragma unroll
+      for (int nq = 0; nq < NT; ++nq) {
+        const float cA = __shfl_sync(0xffffffffu, corr[nq], (2 * t) * 4);
+        const float cB = __shfl_sync(0xffffffffu, corr[nq], (2 * t + 1) * 4);
+  #pragma unroll
+        for (int mt = 0; mt < T::MT; ++mt) {
+          oacc[mt][nq][0] *= cA;
+          oacc[mt][nq][1] *= cB;
+          oacc[mt][nq][2] *= cA;
+          oacc[mt][nq][3] *= cB;
+        }
       }
-    }
+      }
     }
 
     // ---- O^T += V_hat^T P^T ---------------------------------------------
@@ -510,16 +641,32 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
   if constexpr (!BULK) cp_async_wait<0>();
 
   // ---- combine the warps ------------------------------------------------
+  if constexpr (NT == 1) {  // rows 2t, 2t+1: sum over the 8 lanes of the same t
 #pragma unroll
-  for (int hf = 0; hf < NT; ++hf) {
-    l_run[hf] += __shfl_xor_sync(0xffffffffu, l_run[hf], 1);
-    l_run[hf] += __shfl_xor_sync(0xffffffffu, l_run[hf], 2);
+    for (int k = 0; k < 2; ++k) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) lrow[k] += __shfl_xor_sync(0xffffffffu, lrow[k], o);
+    }
+  } else {
+#pragma unroll
+    for (int hf = 0; hf < NT; ++hf) {
+      l_run[hf] += __shfl_xor_sync(0xffffffffu, l_run[hf], 1);
+      l_run[hf] += __shfl_xor_sync(0xffffffffu, l_run[hf], 2);
+    }
   }
   __syncthreads();  // every warp is done with its pipeline buffers
   float* sO = reinterpret_cast<float*>(pipe);           // [WARPS][RB][DV]
   float* sM = sO + WARPS * T::RB * DV;                  // [WARPS][RB]
   float* sL = sM + WARPS * T::RB;                       // [WARPS][RB]
-  if (t == 0) {
+  if constexpr (NT == 1) {
+    if (g == 0) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        sM[warp * T::RB + 2 * t + k] = mrow[k];
+        sL[warp * T::RB + 2 * t + k] = lrow[k];
+      }
+    }
+  } else if (t == 0) {
 #pragma unroll
     for (int hf = 0; hf < NT; ++hf) {
       sM[warp * T::RB + 8 * hf + g] = m_run[hf];

@@ -150,6 +150,14 @@ __device__ __forceinline__ uint32_t bcast_hi(uint32_t x) {
   return __byte_perm(x, x, 0x3232);
 }
 
+// Transpose of an 8 x 8 matrix of 16-bit values held one row pair per lane
+// (lane 4r + c holds elements (r, 2c) and (r, 2c+1)).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t r;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(r) : "r"(x));
+  return r;
+}
+
 // Two f32 -> f16x2 (round to nearest even), lo from a.
 __device__ __forceinline__ uint32_t f32x2_to_f16x2(float a, float b) {
   uint32_t r;
