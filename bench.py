@@ -273,12 +273,17 @@ def run_gpu(args, world, rank, local):
     # ---- end to end through the public API with host buffers -------------
     pin = lambda t: t.contiguous().pin_memory()
     h_q, h_k, h_v = pin(batch.q), pin(batch.new.k[order]), pin(batch.new.v[order])
+    h_b, h_p = pin(batch.new.batch_idx[order]), pin(batch.new.positions[order])
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(row_k), torch.empty_like(row_v)
+    d_b, d_p = torch.empty_like(new_b), torch.empty_like(new_p)
+    # the two-launch step also needs the new tokens' request and position
+    ins = [(d_q, h_q), (d_k, h_k), (d_v, h_v)] + (
+        [(d_b, h_b), (d_p, h_p)] if args.separate_append else [])
     ws = plan.workspace
     e2e_steps = max(3, min(args.steps, 200))
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v))
+    h2d = sum(h.numel() * h.element_size() for _, h in ins)
     h2d += int(plan.info.plan_host_bytes) + 4
     d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
     times = []
@@ -286,14 +291,19 @@ def run_gpu(args, world, rank, local):
         flush.fill_(1)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v)):
+        for d, h in ins:
             d.copy_(h, non_blocking=True)
         p2 = N.nvfp4kv_decode_plan(batch.qo_indptr, batch.kv_indptr, batch.last_page_len,
                                    c.num_qo_heads, c.num_kv_heads, c.head_dim_qk,
                                    c.head_dim_vo, causal=c.causal, kernel=args.kernel,
                                    device=local, reuse=plan)
-        N.nvfp4kv_decode_append_run(p2, d_k, d_v, d_q, cache, kv_indices, batch.sm_scale,
-                                    out=out, lse=lse)
+        if args.separate_append:
+            N.nvfp4kv_quantize_append(cache, d_k, d_v, d_b, d_p, kv_indices, kv_indptr, last,
+                                      device_flags=flags)
+            N.nvfp4kv_decode_run(p2, d_q, cache, kv_indices, batch.sm_scale, out=out, lse=lse)
+        else:
+            N.nvfp4kv_decode_append_run(p2, d_k, d_v, d_q, cache, kv_indices, batch.sm_scale,
+                                        out=out, lse=lse)
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
         stream.synchronize()
@@ -471,6 +481,8 @@ def main():
     ap.add_argument("--separate-append", action="store_true",
                     help="quantize_append and decode_run as two launches per step")
     args = ap.parse_args()
+    if args.kernel == 2:  # the CUDA-core comparison kernel has no fused append
+        args.separate_append = True
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world, rank, local = init_dist()

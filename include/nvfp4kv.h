@@ -69,8 +69,10 @@ typedef enum nvfp4kv_status {
 /* Bits of the device flag word (see nvfp4kv_workspace_flags). */
 #define NVFP4KV_FLAG_BAD_PAGE_INDEX 0x1u   /* a kv_indices entry out of pool  */
 #define NVFP4KV_FLAG_BAD_APPEND_TARGET 0x2u /* append token outside its request */
-#define NVFP4KV_FLAG_COPY_TIMEOUT 0x4u  /* a page copy did not complete in time;
-                                           the affected rows are not valid   */
+#define NVFP4KV_FLAG_COPY_TIMEOUT 0x4u  /* a pipeline wait of the tcgen05 kernel
+                                           ran out (a copy or product did not
+                                           complete in time); the affected
+                                           rows are not valid                */
 
 const char* nvfp4kv_status_string(int status);
 const char* nvfp4kv_last_error_detail(void);

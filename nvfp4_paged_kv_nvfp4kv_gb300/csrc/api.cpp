@@ -15,7 +15,7 @@
 #include "internal.h"
 
 namespace nvfp4kv {
-bool attend_config_tc(int dk, int dv, int rows, bool bulk, AttendConfig* cfg);
+bool attend_config_tc(int dk, int dv, int rows, AttendConfig* cfg);
 bool attend_config_simt(int dk, int dv, int rows, AttendConfig* cfg);
 bool attend_config_tcgen05(int dk, int dv, int rows, AttendConfig* cfg);
 cudaError_t prepare_kernel(const AttendConfig& cfg);
@@ -133,26 +133,11 @@ CacheView view_of(const nvfp4kv_paged_cache* c) {
   return v;
 }
 
-bool lookup_kernel(int kind, int dk, int dv, int rows, bool bulk, AttendConfig* cfg) {
-  if (kind == kKernelTensorCore) return attend_config_tc(dk, dv, rows, bulk, cfg);
+bool lookup_kernel(int kind, int dk, int dv, int rows, AttendConfig* cfg) {
+  if (kind == kKernelTensorCore) return attend_config_tc(dk, dv, rows, cfg);
   if (kind == kKernelCudaCore) return attend_config_simt(dk, dv, rows, cfg);
   if (kind == kKernelTcgen05) return attend_config_tcgen05(dk, dv, rows, cfg);
   return false;
-}
-
-// The rows of one (page, head) are contiguous in all four buffers and every
-// (page, head) block starts 16-byte aligned: pages can move by bulk copies.
-bool bulk_eligible(const nvfp4kv_paged_cache* c) {
-  auto ok = [](const void* base, int64_t sp, int64_t ss, int64_t sh, int64_t row) {
-    return ss == row && sp % 16 == 0 && sh % 16 == 0 && (16 * row) % 16 == 0 &&
-           reinterpret_cast<uintptr_t>(base) % 16 == 0;
-  };
-  return ok(c->k_data, c->k_stride_page, c->k_stride_slot, c->k_stride_head, c->head_dim_qk / 2) &&
-         ok(c->v_data, c->v_stride_page, c->v_stride_slot, c->v_stride_head, c->head_dim_vo / 2) &&
-         ok(c->k_sf, c->k_sf_stride_page, c->k_sf_stride_slot, c->k_sf_stride_head,
-            c->head_dim_qk / 16) &&
-         ok(c->v_sf, c->v_sf_stride_page, c->v_sf_stride_slot, c->v_sf_stride_head,
-            c->head_dim_vo / 16);
 }
 
 constexpr int kMinChunkPages = 8;
@@ -305,9 +290,8 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
   if (kind == 0)
     kind = (head_dim_qk == 128 && head_dim_vo == 128 && max_rows > 16) ? kKernelTcgen05
                                                                        : kKernelTensorCore;
-  // occupancy is sized on the bulk-copy variant (the contiguous-page path)
   const int want_rows = kind == kKernelTcgen05 ? std::max(max_rows, 1) : (max_rows <= 8 ? 8 : 16);
-  if (!lookup_kernel(kind, head_dim_qk, head_dim_vo, want_rows, true, &cfg))
+  if (!lookup_kernel(kind, head_dim_qk, head_dim_vo, want_rows, &cfg))
     return fail(NVFP4KV_ERR_UNSUPPORTED, "no %s kernel for head dims (%d, %d)",
                 kind == kKernelTensorCore ? "tensor-core"
                 : kind == kKernelTcgen05  ? "tcgen05"
@@ -563,7 +547,7 @@ int attend(const nvfp4kv_plan_info* info, const void* q_bf16, int64_t q_stride_t
   if (info->num_units == 0) return ok();
   AttendConfig cfg{};
   if (!lookup_kernel(info->kernel, info->head_dim_qk, info->head_dim_vo, info->rows_per_block,
-                     bulk_eligible(cache), &cfg))
+                     &cfg))
     return fail(NVFP4KV_ERR_UNSUPPORTED, "planned kernel not available");
   cudaError_t e = prepare_kernel(cfg);
   if (e != cudaSuccess) return cuda_fail(e, "kernel attributes");

@@ -49,8 +49,7 @@ __device__ __forceinline__ void append_unit_tokens(const AttendParams& p, const 
     *reinterpret_cast<uint2*>(drow + 8 * jb) = packed;
     srow[jb] = static_cast<uint8_t>(sfb);
   }
-  __threadfence();
-  dev::fence_proxy_async_global();  // before bulk (async proxy) copies read them
+  __threadfence();  // before other CTAs' copies of the page read them
 }
 
 }  // namespace nvfp4kv

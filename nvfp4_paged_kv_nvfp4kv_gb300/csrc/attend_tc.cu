@@ -56,9 +56,9 @@ using namespace dev;
 #define NVFP4KV_TC_QREGS 1
 #endif
 
-template <int DK, int DV, int NT, int WARPS, int STAGES, bool BULK>
-struct TcTraits : PageStage<DK, DV, BULK> {
-  using S = PageStage<DK, DV, BULK>;
+template <int DK, int DV, int NT, int WARPS, int STAGES>
+struct TcTraits : PageStage<DK, DV> {
+  using S = PageStage<DK, DV>;
   static constexpr int RB = 8 * NT;                  // query rows per CTA
   static constexpr int CB = (DK / 8 < 16) ? DK / 8 : 16;  // K bytes per lane chunk
   static constexpr int NCH = (DK / 8) / CB;          // K chunks per lane
@@ -71,8 +71,7 @@ struct TcTraits : PageStage<DK, DV, BULK> {
   static constexpr int MAIN_BYTES = PIPE_BYTES > COMB_BYTES ? PIPE_BYTES : COMB_BYTES;
   static constexpr int QROW = DK + 8;                // f16 elements, padded
   static constexpr int Q_BYTES = RB * QROW * 2;
-  static constexpr int BAR_BYTES = WARPS * STAGES * 8;  // one mbarrier per stage
-  static constexpr int SMEM = MAIN_BYTES + Q_BYTES + RB * 16 + BAR_BYTES;
+  static constexpr int SMEM = MAIN_BYTES + Q_BYTES + RB * 16;
   static constexpr bool Q_IN_REGS = NVFP4KV_TC_QREGS && KSTEPS * 2 * NT <= 32;
   static_assert(S::VC == VC, "V lane chunk");
 };
@@ -91,13 +90,10 @@ constexpr int tc_min_blocks() {
 // by more than this (log2 domain), so p <= 2^kRaiseLog2 fits f16.
 constexpr float kRaiseLog2 = 8.f;
 
-// Polls of a stage's barrier before the kernel gives up on a bulk copy.
-constexpr uint32_t kWaitLimit = 1u << 20;
-
-template <int DK, int DV, int NT, int WARPS, int STAGES, bool BULK>
+template <int DK, int DV, int NT, int WARPS, int STAGES>
 __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
     attend_tc_kernel(const AttendParams p) {
-  using T = TcTraits<DK, DV, NT, WARPS, STAGES, BULK>;
+  using T = TcTraits<DK, DV, NT, WARPS, STAGES>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* pipe = smem;
   uint16_t* sQ = reinterpret_cast<uint16_t*>(smem + T::MAIN_BYTES);
@@ -154,16 +150,6 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
   // ---- start the page pipeline: the first pages' copies are in flight
   // while Q is prepared ---------------------------------------------------
   uint8_t* wpipe = pipe + warp * STAGES * T::STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::MAIN_BYTES + T::Q_BYTES + T::RB * 16) +
-                   warp * STAGES;
-  if constexpr (BULK) {
-    if (lane == 0) {
-#pragma unroll
-      for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
-      mbar_init_fence();
-    }
-    __syncwarp();
-  }
   const int npw = u.num_pages > warp ? (u.num_pages - warp + WARPS - 1) / WARPS : 0;
   const int32_t* pidx = p.kv_indices + u.page_begin;
 
@@ -177,20 +163,14 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
       if (lane == 0) atomicOr(p.flags, 0x1u);
       pid = 0;
     }
-    if constexpr (BULK) {
-      if (lane == 0)
-        issue_page_bulk<typename T::S>(wpipe + (i % STAGES) * T::STAGE_BYTES,
-                                       &bars[i % STAGES], p.cache, pid, u.h_kv);
-    } else {
-      issue_page<typename T::S>(wpipe + (i % STAGES) * T::STAGE_BYTES, p.cache, pid, u.h_kv,
-                                lane);
-    }
+    issue_page<typename T::S>(wpipe + (i % STAGES) * T::STAGE_BYTES, p.cache, pid, u.h_kv,
+                              lane);
   };
 
 #pragma unroll
   for (int s = 0; s < STAGES - 1; ++s) {
     if (s < npw) load_page(s, page_id(s));
-    if constexpr (!BULK) cp_async_commit();
+    cp_async_commit();
   }
   int32_t next_pid = page_id(STAGES - 1);
   if (new_lo < new_hi && !append_early) append_new();  // ordered by the barrier below
@@ -315,21 +295,8 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
   for (int i = 0; i < npw; ++i) {
     if (i + STAGES - 1 < npw) load_page(i + STAGES - 1, next_pid);
     next_pid = page_id(i + STAGES);
-    if constexpr (BULK) {
-      const bool ok = mbar_wait_bounded(&bars[i % STAGES], (i / STAGES) & 1, kWaitLimit);
-      if (!__all_sync(0xffffffffu, ok)) {
-        // a copy did not land: flag it, wait (bounded) for the copies this
-        // warp still has in flight, and finish without the remaining pages
-        if (lane == 0) atomicOr(p.flags, 0x4u);
-        const int last = min(npw, i + STAGES) - 1;
-        for (int j = i + 1; j <= last; ++j)
-          mbar_wait_bounded(&bars[j % STAGES], (j / STAGES) & 1, kWaitLimit);
-        break;
-      }
-    } else {
-      cp_async_commit();
-      cp_async_wait<STAGES - 1>();
-    }
+    cp_async_commit();
+    cp_async_wait<STAGES - 1>();
     __syncwarp();
     const uint8_t* st = wpipe + (i % STAGES) * T::STAGE_BYTES;
     const int tok0 = u.tok_begin + (warp + i * WARPS) * 16;
@@ -638,7 +605,7 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
     }
     __syncwarp();
   }
-  if constexpr (!BULK) cp_async_wait<0>();
+  cp_async_wait<0>();
 
   // ---- combine the warps ------------------------------------------------
   if constexpr (NT == 1) {  // rows 2t, 2t+1: sum over the 8 lanes of the same t
@@ -697,11 +664,11 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
 #define NVFP4KV_TC_STAGES 4
 #endif
 
-template <int DK, int DV, int NT, bool BULK>
+template <int DK, int DV, int NT>
 bool make_tc(AttendConfig* cfg) {
   constexpr int WARPS = NVFP4KV_TC_WARPS;
   constexpr int STAGES = DK >= 512 ? 3 : NVFP4KV_TC_STAGES;
-  using T = TcTraits<DK, DV, NT, WARPS, STAGES, BULK>;
+  using T = TcTraits<DK, DV, NT, WARPS, STAGES>;
   cfg->kind = kKernelTensorCore;
   cfg->dk = DK;
   cfg->dv = DV;
@@ -709,20 +676,16 @@ bool make_tc(AttendConfig* cfg) {
   cfg->warps = WARPS;
   cfg->smem_bytes = T::SMEM;
   cfg->func =
-      reinterpret_cast<const void*>(attend_tc_kernel<DK, DV, NT, WARPS, STAGES, BULK>);
+      reinterpret_cast<const void*>(attend_tc_kernel<DK, DV, NT, WARPS, STAGES>);
   return true;
 }
 
 }  // namespace
 
-bool attend_config_tc(int dk, int dv, int rows, bool bulk, AttendConfig* cfg) {
+bool attend_config_tc(int dk, int dv, int rows, AttendConfig* cfg) {
   const int nt = rows <= 8 ? 1 : 2;
-#define NVFP4KV_TC_CASE(DK_, DV_)                                             \
-  if (dk == DK_ && dv == DV_) {                                               \
-    if (bulk) return nt == 1 ? make_tc<DK_, DV_, 1, true>(cfg)                \
-                             : make_tc<DK_, DV_, 2, true>(cfg);               \
-    return nt == 1 ? make_tc<DK_, DV_, 1, false>(cfg) : make_tc<DK_, DV_, 2, false>(cfg); \
-  }
+#define NVFP4KV_TC_CASE(DK_, DV_)                                                   \
+  if (dk == DK_ && dv == DV_) return nt == 1 ? make_tc<DK_, DV_, 1>(cfg) : make_tc<DK_, DV_, 2>(cfg);
   NVFP4KV_TC_CASE(64, 64)
   NVFP4KV_TC_CASE(128, 128)
   NVFP4KV_TC_CASE(256, 256)

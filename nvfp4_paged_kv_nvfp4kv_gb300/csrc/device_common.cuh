@@ -37,19 +37,14 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
-// ---- mbarrier + bulk copy (cp.async.bulk, completion counted in bytes) ----
+// ---- mbarrier ----
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_addr(bar)), "r"(count));
 }
-// make the initialised barriers visible to the bulk-copy (async) proxy
+// make the initialised barriers visible to the async proxy (tcgen05.commit)
 __device__ __forceinline__ void mbar_init_fence() {
   asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_addr(bar)),
-               "r"(bytes)
-               : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -60,28 +55,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "r"(smem_addr(bar)), "r"(parity)
       : "memory");
   return ok != 0;
-}
-// Wait for the phase with the given parity to complete, giving up after
-// `limit` polls (each poll may suspend the thread for a short while).
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  uint32_t limit) {
-  for (uint32_t it = 0; it < limit; ++it)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
-// order this thread's global stores before later async-proxy (bulk copy)
-// reads of the same memory
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;\n" ::: "memory");
-}
-// global -> shared bulk copy; `bytes` and both addresses are multiples of 16
-__device__ __forceinline__ void bulk_g2s(void* smem, const void* gmem, uint32_t bytes,
-                                         uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-      "[%3];\n" ::"r"(smem_addr(smem)),
-      "l"(gmem), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
 }
 
 // Four packed bytes (8 e2m1 codes) -> four f16x2: h[j] holds byte j, its low

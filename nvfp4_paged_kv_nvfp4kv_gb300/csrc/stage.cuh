@@ -10,21 +10,19 @@
 namespace nvfp4kv {
 
 // Stage layout: packed K rows [16][Dk/2], K scale rows [16][Dk/16], packed V
-// rows [16][Dv/2 (+16)], V scale rows [16][Dv/16]; every section starts
-// 16-byte aligned.  Filled by per-lane cp.async (BULK = false), odd K rows are
-// xor-swizzled by 4 chunks when Dk >= 256 (a lane quad's 16-byte reads of two
-// rows then hit different banks) and V rows are padded by 16 bytes (the PV
-// reads of lane group g at tokens 2t.. hit distinct banks).  Filled by bulk
-// copies (BULK = true), each section is the page's contiguous bytes as they
-// are in memory.
-template <int DK, int DV, bool BULK = false>
+// rows [16][Dv/2 + 16], V scale rows [16][Dv/16]; every section starts
+// 16-byte aligned.  Filled by per-lane cp.async: odd K rows are xor-swizzled
+// by 4 chunks when Dk >= 256 (a lane quad's 16-byte reads of two rows then
+// hit different banks) and V rows are padded by 16 bytes (the PV reads of
+// lane group g at tokens 2t.. hit distinct banks).  Bulk copies of a page's
+// contiguous bytes (no padding, no swizzle) measured slower.
+template <int DK, int DV>
 struct PageStage {
-  static constexpr bool kBulk = BULK;
   static constexpr int KROW = DK / 2;
-  static constexpr bool KSWZ = !BULK && DK >= 256;
+  static constexpr bool KSWZ = DK >= 256;
   static constexpr int KSFROW = DK / 16;
   static constexpr int VC = DV / 16;
-  static constexpr int VROW = DV / 2 + (BULK ? 0 : 16);
+  static constexpr int VROW = DV / 2 + 16;
   static constexpr int VSFROW = DV / 16;
   static constexpr int K_BYTES = 16 * KROW;
   static constexpr int KSF_BYTES = 16 * KSFROW;
@@ -79,20 +77,6 @@ __device__ __forceinline__ void issue_page(uint8_t* st, const CacheView& c, int3
     cp_async_small<VSU>(st + S::OFF_VSF + r * S::VSFROW + u * VSU,
                         vsb + r * c.vsf_ss + u * VSU);
   }
-}
-
-// Bulk variant: lane 0 arms the stage's barrier with the page's byte count
-// and issues one bulk copy per section (rows of a (page, head) contiguous).
-template <class S>
-__device__ __forceinline__ void issue_page_bulk(uint8_t* st, uint64_t* bar, const CacheView& c,
-                                                int32_t pid, int h) {
-  using namespace dev;
-  constexpr uint32_t kBytes = S::K_BYTES + S::KSF_BYTES + S::V_BYTES + S::VSF_BYTES;
-  mbar_arrive_expect_tx(bar, kBytes);
-  bulk_g2s(st, c.k_data + pid * c.k_sp + h * c.k_sh, S::K_BYTES, bar);
-  bulk_g2s(st + S::OFF_KSF, c.k_sf + pid * c.ksf_sp + h * c.ksf_sh, S::KSF_BYTES, bar);
-  bulk_g2s(st + S::OFF_V, c.v_data + pid * c.v_sp + h * c.v_sh, S::V_BYTES, bar);
-  bulk_g2s(st + S::OFF_VSF, c.v_sf + pid * c.vsf_sp + h * c.vsf_sh, S::VSF_BYTES, bar);
 }
 
 }  // namespace nvfp4kv
