@@ -264,6 +264,26 @@ int nvfp4kv_decode_merge(const nvfp4kv_plan_info* info, void* workspace,
                          uint64_t workspace_bytes, void* out_bf16, float* lse,
                          cudaStream_t stream);
 
+/* ---- dequantise ------------------------------------------------------------ */
+/* Paged NVFP4 -> float32 for a list of pages (the cache format of page
+ * "Support NVFP4 KV cache decode on SM120"; page "Re-enable split-KV for
+ * NVFP4 KV cache in prefill path" checks attention against such a dequantised
+ * copy): x_hat = e2m1(code) * E4M3(scale) * global_scale, the exact value
+ * rounded to float32 (code * scale is exact; one rounding).
+ *   page_ids [dev] int32 [num_ids]: physical page of each entry;
+ *   k_out [dev, may be NULL] float32 [num_ids, 16, num_kv_heads, head_dim_qk]:
+ *     element (e, slot, h, d) = K of page page_ids[e], slot, head h, dim d;
+ *   v_out [dev, may be NULL] float32 [num_ids, 16, num_kv_heads, head_dim_vo];
+ *   device_flags [dev, may be NULL]: NVFP4KV_FLAG_BAD_PAGE_INDEX is or-ed in
+ *     for an id outside [0, num_pages); that entry's slots are written as 0.
+ * Every slot of a page is converted, including slots past a request's
+ * length (they hold whatever the pool held).  Outputs are 16-byte aligned;
+ * any cache accepted by nvfp4kv_quantize_append is accepted.  Enqueued on
+ * `stream`; nothing is allocated. */
+int nvfp4kv_dequantize_paged(const nvfp4kv_paged_cache* cache, const int32_t* page_ids,
+                             int32_t num_ids, float* k_out, float* v_out,
+                             uint32_t* device_flags, cudaStream_t stream);
+
 /* ---- merge ---------------------------------------------------------------- */
 /* Fold partial attention states (the flash-decoding split of page
  * "Re-enable split-KV for NVFP4 KV cache in prefill path"; the pages give no

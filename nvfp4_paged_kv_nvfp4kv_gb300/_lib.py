@@ -66,6 +66,8 @@ SIGNATURES = {
     "nvfp4kv_quantize_append": (C.c_int, [
         C.POINTER(PagedCacheStruct), _vp, _i64, _i64, _vp, _i64, _i64, _i32, _vp, _vp,
         _vp, _vp, _vp, _i32, _vp, _vp]),
+    "nvfp4kv_dequantize_paged": (C.c_int, [
+        C.POINTER(PagedCacheStruct), _vp, _i32, _vp, _vp, _vp, _vp]),
     "nvfp4kv_decode_plan": (C.c_int, [
         _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, C.POINTER(PlanOptions), _i32,
         _vp, _u64, _vp, _u64, _vp, C.POINTER(PlanInfo)]),

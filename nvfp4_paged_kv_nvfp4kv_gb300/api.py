@@ -18,7 +18,8 @@ from ._lib import NvFp4KvError, PagedCacheStruct, PlanInfo, PlanOptions, check
 __all__ = ["PagedCache", "Plan", "NvFp4KvError", "nvfp4kv_quantize_append",
            "nvfp4kv_decode_plan", "nvfp4kv_decode_run", "nvfp4kv_decode_attend",
            "nvfp4kv_decode_merge", "nvfp4kv_merge_states", "nvfp4kv_workspace_flags",
-           "nvfp4kv_decode_run_static", "nvfp4kv_decode_append_run"]
+           "nvfp4kv_decode_run_static", "nvfp4kv_decode_append_run",
+           "nvfp4kv_dequantize_paged"]
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -98,6 +99,28 @@ def nvfp4kv_quantize_append(cache: PagedCache, k: torch.Tensor, v: torch.Tensor,
         _ptr(kv_indices), _ptr(kv_indptr), _ptr(last_page_len),
         int(kv_indptr.numel()) - 1, _ptr(device_flags), _stream(stream))
     check(st, "nvfp4kv_quantize_append")
+
+
+def nvfp4kv_dequantize_paged(cache: PagedCache, page_ids, k_out=None, v_out=None,
+                             want_k=True, want_v=True, device_flags=None, stream=None):
+    """Dequantise the listed pages to float32: returns (k, v), each
+    [len(page_ids), 16, Hkv, D] (or None when not wanted)."""
+    L = _lib.load()
+    n = int(page_ids.numel())
+    dev = cache.k_data.device
+    if want_k and k_out is None:
+        k_out = torch.empty((n, 16, cache.num_kv_heads, cache.head_dim_qk),
+                            dtype=torch.float32, device=dev)
+    if want_v and v_out is None:
+        v_out = torch.empty((n, 16, cache.num_kv_heads, cache.head_dim_vo),
+                            dtype=torch.float32, device=dev)
+    s = cache.struct()
+    st = L.nvfp4kv_dequantize_paged(C.byref(s), _ptr(page_ids), n,
+                                    _ptr(k_out if want_k else None),
+                                    _ptr(v_out if want_v else None), _ptr(device_flags),
+                                    _stream(stream))
+    check(st, "nvfp4kv_dequantize_paged")
+    return (k_out if want_k else None), (v_out if want_v else None)
 
 
 class Plan:

@@ -161,6 +161,40 @@ const char* nvfp4kv_status_string(int status) {
 
 const char* nvfp4kv_last_error_detail(void) { return g_detail.c_str(); }
 
+int nvfp4kv_dequantize_paged(const nvfp4kv_paged_cache* cache, const int32_t* page_ids,
+                             int32_t num_ids, float* k_out, float* v_out,
+                             uint32_t* device_flags, cudaStream_t stream) {
+  if (int st = check_cache(cache, false)) return st;
+  if (num_ids < 0) return fail(NVFP4KV_ERR_INVALID_ARGUMENT, "num_ids %d negative", num_ids);
+  if (num_ids == 0 || (!k_out && !v_out)) return ok();
+  if (!page_ids) return fail(NVFP4KV_ERR_INVALID_ARGUMENT, "page_ids is null");
+  if ((k_out && !aligned(k_out, 16)) || (v_out && !aligned(v_out, 16)))
+    return fail(NVFP4KV_ERR_INVALID_ARGUMENT, "outputs must be 16-byte aligned");
+  DequantParams p{};
+  p.k_data = cache->k_data; p.v_data = cache->v_data;
+  p.k_sf = cache->k_sf; p.v_sf = cache->v_sf;
+  p.k_sp = cache->k_stride_page; p.k_ss = cache->k_stride_slot; p.k_sh = cache->k_stride_head;
+  p.v_sp = cache->v_stride_page; p.v_ss = cache->v_stride_slot; p.v_sh = cache->v_stride_head;
+  p.ksf_sp = cache->k_sf_stride_page; p.ksf_ss = cache->k_sf_stride_slot;
+  p.ksf_sh = cache->k_sf_stride_head;
+  p.vsf_sp = cache->v_sf_stride_page; p.vsf_ss = cache->v_sf_stride_slot;
+  p.vsf_sh = cache->v_sf_stride_head;
+  p.num_pages = cache->num_pages;
+  p.num_kv_heads = cache->num_kv_heads;
+  p.head_dim_qk = cache->head_dim_qk;
+  p.head_dim_vo = cache->head_dim_vo;
+  p.k_global_scale = cache->k_global_scale;
+  p.v_global_scale = cache->v_global_scale;
+  p.page_ids = page_ids;
+  p.num_ids = num_ids;
+  p.k_out = k_out;
+  p.v_out = v_out;
+  p.flags = device_flags;
+  cudaError_t e = launch_dequantize(p, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dequantize launch");
+  return ok();
+}
+
 int nvfp4kv_quantize_append(const nvfp4kv_paged_cache* cache, const void* k_bf16,
                             int64_t k_stride_tok, int64_t k_stride_head,
                             const void* v_bf16, int64_t v_stride_tok,

@@ -91,6 +91,22 @@ struct AppendParams {
   uint32_t* flags;
 };
 
+struct DequantParams {
+  const uint8_t* k_data;
+  const uint8_t* v_data;
+  const uint8_t* k_sf;
+  const uint8_t* v_sf;
+  int64_t k_sp, k_ss, k_sh, v_sp, v_ss, v_sh;
+  int64_t ksf_sp, ksf_ss, ksf_sh, vsf_sp, vsf_ss, vsf_sh;
+  int32_t num_pages, num_kv_heads, head_dim_qk, head_dim_vo;
+  float k_global_scale, v_global_scale;
+  const int32_t* page_ids;
+  int32_t num_ids;
+  float* k_out;  // [num_ids, 16, Hkv, Dk] or null
+  float* v_out;  // [num_ids, 16, Hkv, Dv] or null
+  uint32_t* flags;
+};
+
 // Kernel families and their launch descriptions (defined in the .cu files).
 enum KernelKind { kKernelTensorCore = 1, kKernelCudaCore = 2, kKernelTcgen05 = 3 };
 
@@ -108,6 +124,7 @@ bool attend_config(int kind, int dk, int dv, int rows, AttendConfig* cfg);
 cudaError_t launch_attend(const AttendConfig& cfg, const AttendParams& p,
                           int grid_x, int grid_y, cudaStream_t stream);
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_dequantize(const DequantParams& p, cudaStream_t stream);
 cudaError_t launch_merge(const float* o_partial, const float* lse_partial,
                          const int32_t* merge_indptr, int32_t num_entries,
                          int32_t head_dim_vo, uint16_t* out, float* lse,

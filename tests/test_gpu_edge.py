@@ -219,3 +219,39 @@ def test_fused_append_small(layout, kw, qo_len, causal):
     H.compare_cache_bytes(g.cache, oc)
     ro, rl = H.oracle_attention(batch, oc, pt)
     H.compare(out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("layout", ["HND", "NHD"])
+@pytest.mark.parametrize("dk,dv", [(128, 128), (512, 256)])
+def test_dequantize_paged_bit_exact(layout, dk, dv):
+    """nvfp4kv_dequantize_paged: every slot of every listed page equals the
+    oracle's exact dequantised value rounded to float32, byte for byte."""
+    batch = small(kv_lens=(17, 40, 161), head_dim_qk=dk, head_dim_vo=dv)
+    g = H.GpuCase(batch, layout=layout)
+    oc, _ = H.oracle_cache(batch, layout)
+    ids = g.kv_indices
+    k, v = N.nvfp4kv_dequantize_paged(g.cache, ids, device_flags=g.flags)
+    torch.cuda.synchronize()
+    assert int(g.flags.item()) == 0
+    k, v = k.cpu().numpy(), v.cpu().numpy()
+    c = batch.cfg
+    for e, page in enumerate(ids.cpu().tolist()):
+        for slot in range(16):
+            for h in range(c.num_kv_heads):
+                rk = O.dequant_row(oc, 0, page, slot, h).astype(np.float32)
+                rv = O.dequant_row(oc, 1, page, slot, h).astype(np.float32)
+                assert np.array_equal(k[e, slot, h].view(np.uint32), rk.view(np.uint32))
+                assert np.array_equal(v[e, slot, h].view(np.uint32), rv.view(np.uint32))
+
+
+def test_dequantize_paged_bad_page_and_partial_outputs():
+    batch = small(kv_lens=(40,))
+    g = H.GpuCase(batch)
+    ids = torch.tensor([int(batch.kv_indices[0]), 10 ** 6, -1], dtype=torch.int32,
+                       device="cuda")
+    k, v = N.nvfp4kv_dequantize_paged(g.cache, ids, want_v=False, device_flags=g.flags)
+    torch.cuda.synchronize()
+    assert v is None
+    assert int(g.flags.item()) & N._lib.FLAG_BAD_PAGE_INDEX
+    assert bool((k[1:] == 0).all())
+    assert bool((k[0].abs().sum() > 0))

@@ -126,3 +126,29 @@ def test_fused_append_run(name):
     H.compare_cache_bytes(g.cache, oc, pages)
     ro, rl = H.oracle_attention(batch, oc, pt, requests)
     H.compare(out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("name", ["long_context_decode", "prefix_cache_extend"])
+def test_amax_global_scales(name):
+    """The long-context decode and prefix-cache extend workloads with
+    per-tensor global scales amax / (6 * 448) (the batched-decode recipe)
+    instead of 1: quantiser bytes identical, attention within tolerance."""
+    import dataclasses
+    cfg = dataclasses.replace(W.WORKLOADS[name], amax_global_scale=True)
+    batch = W.make_batch(cfg)
+    assert batch.k_global_scale != 1.0 and batch.v_global_scale != 1.0
+    requests = None
+    if name == "prefix_cache_extend":
+        order = np.argsort(batch.kv_lens)
+        requests = sorted({int(order[0]), int(order[-1])})
+    g = H.GpuCase(batch)
+    oc, pt = H.oracle_cache(batch, requests=requests)
+    pages = None
+    if requests is not None:
+        kvp = batch.kv_indptr.tolist()
+        pages = sorted({int(batch.kv_indices[i]) for b in requests
+                        for i in range(kvp[b], kvp[b + 1])})
+    H.compare_cache_bytes(g.cache, oc, pages)
+    out, lse = g.run()
+    ro, rl = H.oracle_attention(batch, oc, pt, requests)
+    H.compare(out, lse, ro, rl)
