@@ -219,16 +219,6 @@ __device__ __forceinline__ bool named_or(int id, int n, bool v) {
       : "memory");
   return r != 0;
 }
-__device__ __forceinline__ bool named_and(int id, int n, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n"
-      " selp.u32 %0, 1, 0, q;\n}\n"
-      : "=r"(r)
-      : "r"((uint32_t)v), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
-}
 // One poll that may suspend the thread until the phase completes (or the
 // hinted time, in ns, elapses): waiting warps sleep instead of spinning and
 // leave the issue slots to the warps that work.
@@ -577,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
                              fabsf(bf16_bits_to_f32(w[e] >> 16))));
       atomicMax(&s_qamax[r], __float_as_int(am));
     }
-    named_sync(1, 256);
+    named_sync(3, 256);
     auto exp_of = [&](int r) {  // e with amax * 2^e in [2^14, 2^15)
       const float amax = __int_as_float(s_qamax[r]);
       int e = 0;
@@ -624,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
     }
     fence_async_smem();
     tc_fence_before();
-    named_sync(1, 256);
+    named_sync(3, 256);
     __syncwarp();
     if (lane == 0) mbar_arrive(q_full);
     const int min_lim = *s_minlim;
@@ -655,13 +645,21 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
       }
     };
 
-    bool alive = true;
+    // The two column halves (warps 0-3 and 4-7) are independent groups: each
+    // votes and reduces over its own 128 threads (barrier 1 + half).  A wait
+    // that runs out sets the abort flag; the loop then runs to its end with
+    // every later wait returning at once, so no thread leaves a barrier
+    // sequence the others still follow.
+    const int gbar = 1 + (warp >> 2), gtid = tid & 127;
+    auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
+      bool ok = true;
+      if (lane == 0) ok = wait_bar(bar, parity, s_abort, p.flags);
+      return __shfl_sync(0xffffffffu, ok, 0);
+    };
     for (int i = 0; i < ntiles; ++i) {
       const int sb = i & 1;
-      // thread 0 polls; the group sleeps in the barrier that shares the outcome.
       // S(i) done also means PV(i-2) done: P buffer sb is free again.
-      alive = named_and(1, 256, tid != 0 || wait_bar(&s_full[sb], (i >> 1) & 1, s_abort, p.flags));
-      if (!alive) break;
+      warp_wait(&s_full[sb], (i >> 1) & 1);
       tc_fence_after();
       const int tile_tok0 = u.tok_begin + i * kTileTok;
       const int tok = tile_tok0 + j;
@@ -685,10 +683,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
           for (int e = 0; e < CW; ++e) x[ch * CW + e] = xc[e];
         }
       }
-      if (named_or(1, 256, trig)) {
-        // ---- raise the running maxima to the tile's exact row maxima ----
-        if (tid < N) s_max[tid] = INT32_MIN;
-        named_sync(1, 256);
+      if (named_or(gbar, 128, trig)) {
+        // ---- raise this half's running maxima to the tile's row maxima ----
+        if (gtid < NH) s_max[c0 + gtid] = INT32_MIN;
+        named_sync(gbar, 128);
         if (active) {
 #pragma unroll
           for (int e = 0; e < NH; ++e) {
@@ -696,10 +694,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
             if (lane == 0) atomicMax(&s_max[c0 + e], k);
           }
         }
-        named_sync(1, 256);
+        named_sync(gbar, 128);
         bool moved = false;
-        if (tid < N) {
-          const int r = tid;
+        if (gtid < NH) {
+          const int r = c0 + gtid;
           const float tm = funkey(s_max[r]);  // tile max, relative to the old m_use
           const float m_old = s_m[r];
           float corr = 1.f, delta = 0.f;
@@ -715,32 +713,26 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
           s_corr[r] = corr;
           s_max[r] = __float_as_int(delta);
         }
-        const bool rescale = named_or(1, 256, moved) && i > 0;
+        const bool rescale = named_or(gbar, 128, moved) && i > 0;
 #pragma unroll
         for (int e = 0; e < NH; ++e) x[e] -= __int_as_float(s_max[c0 + e]);
-        if (rescale) {  // O^T and row-sum columns *= corr, once PV(i-1) is done
-          alive = named_and(1, 256,
-                            tid != 0 || wait_bar(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1,
-                                                 s_abort, p.flags));
-          if (!alive) break;
+        if (rescale && active) {  // O^T and row-sum columns *= corr, once PV(i-1) is done
+          warp_wait(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1);
           tc_fence_after();
-          if (active) {
 #pragma unroll
-            for (int blk = 0; blk < 2; ++blk)
+          for (int blk = 0; blk < 2; ++blk)
 #pragma unroll
-              for (int ch = 0; ch < NCH; ++ch) {
-                uint32_t ov[CW];
-                const uint32_t oa =
-                    tmem + lane_base + (blk ? T::LCOL : T::OCOL) + c0 + ch * CW;
-                tmem_ld<CW>(oa, ov);
-                tmem_wait_ld<CW>(ov);
+            for (int ch = 0; ch < NCH; ++ch) {
+              uint32_t ov[CW];
+              const uint32_t oa = tmem + lane_base + (blk ? T::LCOL : T::OCOL) + c0 + ch * CW;
+              tmem_ld<CW>(oa, ov);
+              tmem_wait_ld<CW>(ov);
 #pragma unroll
-                for (int e = 0; e < CW; ++e)
-                  ov[e] = __float_as_uint(__uint_as_float(ov[e]) * s_corr[c0 + ch * CW + e]);
-                tmem_st<CW>(oa, ov);
-              }
-            tmem_wait_st();
-          }
+              for (int e = 0; e < CW; ++e)
+                ov[e] = __float_as_uint(__uint_as_float(ov[e]) * s_corr[c0 + ch * CW + e]);
+              tmem_st<CW>(oa, ov);
+            }
+          tmem_wait_st();
         }
       }
       // ---- p = 2^x: the P^T row segment of this token --------------------
@@ -764,11 +756,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
     }
 
     // ---- epilogue: O^T row of value dim j, this thread's row columns ------
-    if (alive && ntiles > 0)
-      alive = named_and(1, 256,
-                        tid != 0 || wait_bar(&pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1,
-                                             s_abort, p.flags));
-    if (alive) {
+    if (ntiles > 0) warp_wait(&pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1);
+    {
       tc_fence_after();
       constexpr float kLn2 = 0.69314718055994530942f;
       const bool partial = p.split && u.num_splits > 1;
@@ -806,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
         }
       }
       if (partial)
-        merge_if_last<N, DV, 256>(p, u, row0, R, s_fin, tid, [] { named_sync(1, 256); });
+        merge_if_last<N, DV, 256>(p, u, row0, R, s_fin, tid, [] { named_sync(3, 256); });
     }
     tc_fence_before();
   }
