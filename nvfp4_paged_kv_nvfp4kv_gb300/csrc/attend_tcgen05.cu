@@ -656,6 +656,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
       if (lane == 0) ok = wait_bar(bar, parity, s_abort, p.flags);
       return __shfl_sync(0xffffffffu, ok, 0);
     };
+    // Some column of this half has no maximum yet (then each score is tested
+    // against its column's threshold, else all against kRaise at once).
+    bool unset = active;  // group-uniform: every real column starts unset
     for (int i = 0; i < ntiles; ++i) {
       const int sb = i & 1;
       // S(i) done also means PV(i-2) done: P buffer sb is free again.
@@ -672,15 +675,23 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
         for (int ch = 0; ch < NCH; ++ch) {
           float xc[CW];
           scores(ch, sb, tok_ok, mask_rows, tok, xc);
-          const float4* th = reinterpret_cast<const float4*>(s_thr + c0 + ch * CW);
+          if (unset) {
+            const float4* th = reinterpret_cast<const float4*>(s_thr + c0 + ch * CW);
 #pragma unroll
-          for (int e4 = 0; e4 < CW / 4; ++e4) {
-            const float4 t4 = th[e4];
-            trig |= (xc[4 * e4] > t4.x) | (xc[4 * e4 + 1] > t4.y) | (xc[4 * e4 + 2] > t4.z) |
-                    (xc[4 * e4 + 3] > t4.w);
+            for (int e4 = 0; e4 < CW / 4; ++e4) {
+              const float4 t4 = th[e4];
+              trig |= (xc[4 * e4] > t4.x) | (xc[4 * e4 + 1] > t4.y) |
+                      (xc[4 * e4 + 2] > t4.z) | (xc[4 * e4 + 3] > t4.w);
+            }
           }
 #pragma unroll
           for (int e = 0; e < CW; ++e) x[ch * CW + e] = xc[e];
+        }
+        if (!unset) {  // every real column has a maximum: one test of the largest
+          float mx = x[0];
+#pragma unroll
+          for (int e = 1; e < NH; ++e) mx = fmaxf(mx, x[e]);
+          trig = mx > kRaise;
         }
       }
       if (named_or(gbar, 128, trig)) {
@@ -714,6 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
           s_max[r] = __float_as_int(delta);
         }
         const bool rescale = named_or(gbar, 128, moved) && i > 0;
+        unset = named_or(gbar, 128, gtid < NH && c0 + gtid < nvalid && s_m[c0 + gtid] == -INFINITY);
 #pragma unroll
         for (int e = 0; e < NH; ++e) x[e] -= __int_as_float(s_max[c0 + e]);
         if (rescale && active) {  // O^T and row-sum columns *= corr, once PV(i-1) is done
