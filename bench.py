@@ -212,7 +212,8 @@ def run_gpu(args, world, rank, local):
     c = cfg
     plan = N.nvfp4kv_decode_plan(batch.qo_indptr, batch.kv_indptr, batch.last_page_len,
                                  c.num_qo_heads, c.num_kv_heads, c.head_dim_qk, c.head_dim_vo,
-                                 causal=c.causal, kernel=args.kernel, device=local)
+                                 causal=c.causal, kernel=args.kernel, device=local,
+                                 force_chunk_tokens=args.chunk_tokens)
     rows = int(batch.qo_indptr[-1])
     out = torch.empty((rows, c.num_qo_heads, c.head_dim_vo), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((rows, c.num_qo_heads), dtype=torch.float32, device=dev)
@@ -296,6 +297,7 @@ def run_gpu(args, world, rank, local):
         p2 = N.nvfp4kv_decode_plan(batch.qo_indptr, batch.kv_indptr, batch.last_page_len,
                                    c.num_qo_heads, c.num_kv_heads, c.head_dim_qk,
                                    c.head_dim_vo, causal=c.causal, kernel=args.kernel,
+                                   force_chunk_tokens=args.chunk_tokens,
                                    device=local, reuse=plan)
         if args.separate_append:
             N.nvfp4kv_quantize_append(cache, d_k, d_v, d_b, d_p, kv_indices, kv_indptr, last,
@@ -477,6 +479,8 @@ def main():
     ap.add_argument("--workload", default="long_context_decode", choices=list(W.WORKLOADS))
     ap.add_argument("--layout", default="HND", choices=["HND", "NHD"])
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 tensor-core mma.sync, 2 CUDA-core, 3 tcgen05")
+    ap.add_argument("--chunk-tokens", type=int, default=0,
+                    help="split-KV chunk in tokens (multiple of 16); 0 = the planner's choice")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--separate-append", action="store_true",
                     help="quantize_append and decode_run as two launches per step")
