@@ -272,28 +272,41 @@ def run_gpu(args, world, rank, local):
     value = kv_tokens * world / (ms_step_max * 1e-3)
 
     # ---- end to end through the public API with host buffers -------------
-    pin = lambda t: t.contiguous().pin_memory()
-    h_q, h_k, h_v = pin(batch.q), pin(batch.new.k[order]), pin(batch.new.v[order])
-    h_b, h_p = pin(batch.new.batch_idx[order]), pin(batch.new.positions[order])
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(row_k), torch.empty_like(row_v)
-    d_b, d_p = torch.empty_like(new_b), torch.empty_like(new_p)
-    # the two-launch step also needs the new tokens' request and position
-    ins = [(d_q, h_q), (d_k, h_k), (d_v, h_v)] + (
-        [(d_b, h_b), (d_p, h_p)] if args.separate_append else [])
-    ws = plan.workspace
+    # The step's inputs travel in one pinned host buffer and one copy; the
+    # library reads them through 16-byte-aligned slices of one device buffer
+    # (out and lse come back the same way).
+    def packed(tensors, device):
+        offs, n = [], 0
+        for t in tensors:
+            offs.append(n)
+            n += (t.numel() * t.element_size() + 255) // 256 * 256
+        buf = torch.empty(n, dtype=torch.uint8, device=device,
+                          pin_memory=(device == "cpu"))
+        views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                 for o, t in zip(offs, tensors)]
+        return buf, views
+    src = [batch.q, batch.new.k[order].contiguous(), batch.new.v[order].contiguous()]
+    if args.separate_append:  # the two-launch step also needs request and position
+        src += [batch.new.batch_idx[order].contiguous(), batch.new.positions[order].contiguous()]
+    h_in, h_views = packed(src, "cpu")
+    for hv, t in zip(h_views, src):
+        hv.copy_(t)
+    d_in, d_views = packed(src, dev)
+    d_q, d_k, d_v = d_views[:3]
+    d_b, d_p = (d_views[3], d_views[4]) if args.separate_append else (None, None)
+    h_res, (h_out, h_lse) = packed([out, lse], "cpu")
+    d_res, (e_out, e_lse) = packed([out, lse], dev)
     e2e_steps = max(3, min(args.steps, 200))
-    h2d = sum(h.numel() * h.element_size() for _, h in ins)
-    h2d += int(plan.info.plan_host_bytes) + 4
-    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+    # bytes moved per step: the packed buffers (with their alignment padding)
+    # and the plan's work list
+    h2d = h_in.numel() + int(plan.info.plan_host_bytes)
+    d2h = h_res.numel()
     times = []
     for k in range(e2e_steps + 3):
         flush.fill_(1)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for d, h in ins:
-            d.copy_(h, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
         p2 = N.nvfp4kv_decode_plan(batch.qo_indptr, batch.kv_indptr, batch.last_page_len,
                                    c.num_qo_heads, c.num_kv_heads, c.head_dim_qk,
                                    c.head_dim_vo, causal=c.causal, kernel=args.kernel,
@@ -302,15 +315,16 @@ def run_gpu(args, world, rank, local):
         if args.separate_append:
             N.nvfp4kv_quantize_append(cache, d_k, d_v, d_b, d_p, kv_indices, kv_indptr, last,
                                       device_flags=flags)
-            N.nvfp4kv_decode_run(p2, d_q, cache, kv_indices, batch.sm_scale, out=out, lse=lse)
+            N.nvfp4kv_decode_run(p2, d_q, cache, kv_indices, batch.sm_scale, out=e_out,
+                                 lse=e_lse)
         else:
             N.nvfp4kv_decode_append_run(p2, d_k, d_v, d_q, cache, kv_indices, batch.sm_scale,
-                                        out=out, lse=lse)
-        h_out.copy_(out, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+                                        out=e_out, lse=e_lse)
+        h_res.copy_(d_res, non_blocking=True)
         stream.synchronize()
         if k >= 3:
             times.append(time.perf_counter() - t0)
+    assert torch.equal(h_out.view(torch.int16), out.cpu().view(torch.int16))
     e2e_s = max_over_ranks(statistics.mean(times), world)
     e2e_value = kv_tokens * world / e2e_s
 

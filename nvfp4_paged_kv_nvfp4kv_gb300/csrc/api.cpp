@@ -7,7 +7,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include <cuda_runtime_api.h>
@@ -338,11 +341,20 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
     cudaError_t e = cudaSuccess;
     if (dev < 0) e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (num_sms == 0) {
-      e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-      if (e != cudaSuccess) return cuda_fail(e, "SM count");
+    // the device's SM count and the kernel's resident CTAs per SM do not
+    // change: query them once per (device, kernel) and keep them (a plan is
+    // built every serving step)
+    static std::mutex mu;
+    static std::map<std::pair<int, const void*>, std::pair<int, int>> known;
+    std::pair<int, int> sm_occ{0, 0};
+    {
+      std::lock_guard<std::mutex> lock(mu);
+      auto it = known.find({dev, cfg.func});
+      if (it != known.end()) sm_occ = it->second;
     }
-    if (ctas_per_sm == 0) {
+    if (sm_occ.first == 0) {
+      e = cudaDeviceGetAttribute(&sm_occ.first, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return cuda_fail(e, "SM count");
       int optin = 0;
       e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
       if (e != cudaSuccess) return cuda_fail(e, "shared-memory opt-in");
@@ -350,13 +362,22 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
         return fail(NVFP4KV_ERR_UNSUPPORTED,
                     "kernel needs %d bytes of shared memory, device allows %d per block",
                     cfg.smem_bytes, optin);
+      int cur = -1;
+      e = cudaGetDevice(&cur);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+      if (cur != dev && (e = cudaSetDevice(dev)) != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
       e = prepare_kernel(cfg);
-      if (e != cudaSuccess) return cuda_fail(e, "kernel attributes");
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctas_per_sm, cfg.func,
-                                                        cfg.warps * 32, cfg.smem_bytes);
+      if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sm_occ.second, cfg.func,
+                                                          cfg.warps * 32, cfg.smem_bytes);
+      if (cur != dev) cudaSetDevice(cur);
       if (e != cudaSuccess) return cuda_fail(e, "occupancy");
-      if (ctas_per_sm < 1) ctas_per_sm = 1;
+      if (sm_occ.second < 1) sm_occ.second = 1;
+      std::lock_guard<std::mutex> lock(mu);
+      known[{dev, cfg.func}] = sm_occ;
     }
+    if (num_sms == 0) num_sms = sm_occ.first;
+    if (ctas_per_sm == 0) ctas_per_sm = sm_occ.second;
     info->device = dev;
   } else {
     info->device = device;
