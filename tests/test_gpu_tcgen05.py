@@ -105,3 +105,62 @@ def test_tcgen05_workloads(name):
     assert N.nvfp4kv_workspace_flags(g.plan) == 0
     ro, rl = H.oracle_attention(batch, oc, pt, requests)
     H.compare(out, lse, ro, rl)
+
+
+def test_tcgen05_page_order_invariance_with_poison():
+    """Pool bytes 0xFF everywhere outside the written slots (NaN scales in
+    the tail slots and unused pages): results are bit-identical under a
+    permutation of the physical pages, and finite."""
+    batch = small(qo_len=16, causal=True, kv_lens=(37, 300, 1000))
+    b1 = W.make_batch(batch.cfg, extra_pages=9)
+    g1 = H.GpuCase(b1, fill=0xFF, kernel=3, force_chunk_tokens=256)
+    o1, l1 = g1.run()
+    perm = torch.randperm(b1.num_pages, generator=torch.Generator().manual_seed(5))
+    b1.kv_indices = perm[b1.kv_indices.long()].to(torch.int32)
+    g2 = H.GpuCase(b1, fill=0xFF, kernel=3, force_chunk_tokens=256)
+    o2, l2 = g2.run()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
+    assert not torch.isnan(o1.float()).any()
+
+
+def test_tcgen05_bad_page_index_sets_flag_without_fault():
+    batch = small(qo_len=16, causal=True, kv_lens=(40, 300))
+    g = H.GpuCase(batch, kernel=3)
+    assert N.nvfp4kv_workspace_flags(g.plan, clear=True) == 0
+    bad = g.kv_indices.clone()
+    bad[3] = batch.num_pages + 5
+    rows = int(batch.qo_indptr[-1])
+    out = torch.empty((rows, 8, 128), dtype=torch.bfloat16, device="cuda")
+    N.nvfp4kv_decode_run(g.plan, g.q, g.cache, bad, batch.sm_scale, out=out)
+    torch.cuda.synchronize()
+    assert N.nvfp4kv_workspace_flags(g.plan, clear=True) & 0x1
+    out2, _ = g.run()  # the context still works and the good table is clean
+    assert N.nvfp4kv_workspace_flags(g.plan) == 0
+    assert not torch.isnan(out2.float()).any()
+
+
+def test_tcgen05_causal_rows_that_start_late_in_a_split():
+    """Short chunks over the new tokens: in the last units some query rows
+    see no token of the first tile (their maximum is set on a later tile)."""
+    batch = small(qo_len=16, causal=True, kv_lens=(16, 140, 395))
+    check(batch, force_chunk_tokens=128)
+    check(batch, force_chunk_tokens=256)
+
+
+def test_tcgen05_v_ones_and_q_zero_probes():
+    batch = small(qo_len=16, causal=True, kv_lens=(37, 100, 250))
+    for ts in (batch.prefix, batch.new):
+        ts.v.fill_(1.0)
+    batch.q.zero_()
+    g = H.GpuCase(batch, kernel=3, force_chunk_tokens=128)
+    out, lse = g.run()
+    assert torch.all(out.float() == 1.03125)
+    # uniform scores: lse = ln(number of visible keys) for every row
+    import math
+    want = []
+    for b, L in enumerate(batch.kv_lens):
+        for i in range(16):
+            want.append([math.log(L - 16 + i + 1)] * 8)
+    want = torch.tensor(want, device="cuda", dtype=torch.float32)
+    assert torch.allclose(lse, want, atol=1e-5, rtol=0)
