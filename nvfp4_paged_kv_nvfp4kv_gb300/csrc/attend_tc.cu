@@ -300,6 +300,46 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
     __syncwarp();
     const uint8_t* st = wpipe + (i % STAGES) * T::STAGE_BYTES;
     const int tok0 = u.tok_begin + (warp + i * WARPS) * 16;
+    // V rows and scales of this page, loaded before the score product
+    const uint8_t* vrow = st + T::OFF_V + g * T::VC;
+    const int tk[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+    constexpr int VW = T::VC / 4 > 0 ? T::VC / 4 : 1;  // 32-bit words per lane
+    uint32_t vw[4][VW];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint8_t* src = vrow + tk[k] * T::VROW;
+      if constexpr (T::VC == 16) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src);
+        vw[k][0] = v.x; vw[k][1] = v.y; vw[k][2] = v.z; vw[k][3] = v.w;
+      } else if constexpr (T::VC == 8) {
+        const uint2 v = *reinterpret_cast<const uint2*>(src);
+        vw[k][0] = v.x; vw[k][1] = v.y;
+      } else {
+        vw[k][0] = *reinterpret_cast<const uint32_t*>(src);
+      }
+    }
+    // per-token scale pairs for each scale block the lane's bytes touch
+    // Slots past kv_len on the request's last page hold whatever the pool
+    // held (possibly a NaN scale byte); their p is 0, but 0 * NaN would
+    // still poison the product, so their V scales are forced to 0.
+    const int valid = u.kv_len - tok0;  // tokens of this page that exist
+    constexpr int NBL = (T::VC * 2 + 15) / 16;
+    uint32_t sA[NBL], sB[NBL];
+#pragma unroll
+    for (int bl = 0; bl < NBL; ++bl) {
+      const int blk = (g * T::VC * 2) / 16 + bl;
+      const uint8_t* sfs = st + T::OFF_VSF + blk;
+      uint32_t s0 = sfs[tk[0] * T::VSFROW], s1 = sfs[tk[1] * T::VSFROW];
+      uint32_t s2 = sfs[tk[2] * T::VSFROW], s3 = sfs[tk[3] * T::VSFROW];
+      if (valid < 16) {
+        if (tk[0] >= valid) s0 = 0;
+        if (tk[1] >= valid) s1 = 0;
+        if (tk[2] >= valid) s2 = 0;
+        if (tk[3] >= valid) s3 = 0;
+      }
+      sA[bl] = e4m3x2_to_f16x2(s0 | (s1 << 8));
+      sB[bl] = e4m3x2_to_f16x2(s2 | (s3 << 8));
+    }
 
     uint32_t pfrag[NT][2];
     // K row `row` (a token of the page), 16-byte chunk ch of this lane
@@ -529,45 +569,6 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
     // ---- O^T += V_hat^T P^T ---------------------------------------------
     // tokens 2t, 2t+1, 2t+8, 2t+9; lane group g owns bytes [g*VC, g*VC+VC)
     {
-      const uint8_t* vrow = st + T::OFF_V + g * T::VC;
-      const int tk[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
-      constexpr int VW = T::VC / 4 > 0 ? T::VC / 4 : 1;  // 32-bit words per lane
-      uint32_t vw[4][VW];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint8_t* src = vrow + tk[k] * T::VROW;
-        if constexpr (T::VC == 16) {
-          const uint4 v = *reinterpret_cast<const uint4*>(src);
-          vw[k][0] = v.x; vw[k][1] = v.y; vw[k][2] = v.z; vw[k][3] = v.w;
-        } else if constexpr (T::VC == 8) {
-          const uint2 v = *reinterpret_cast<const uint2*>(src);
-          vw[k][0] = v.x; vw[k][1] = v.y;
-        } else {
-          vw[k][0] = *reinterpret_cast<const uint32_t*>(src);
-        }
-      }
-      // per-token scale pairs for each scale block the lane's bytes touch
-      // Slots past kv_len on the request's last page hold whatever the pool
-      // held (possibly a NaN scale byte); their p is 0, but 0 * NaN would
-      // still poison the product, so their V scales are forced to 0.
-      const int valid = u.kv_len - tok0;  // tokens of this page that exist
-      constexpr int NBL = (T::VC * 2 + 15) / 16;
-      uint32_t sA[NBL], sB[NBL];
-#pragma unroll
-      for (int bl = 0; bl < NBL; ++bl) {
-        const int blk = (g * T::VC * 2) / 16 + bl;
-        const uint8_t* sfs = st + T::OFF_VSF + blk;
-        uint32_t s0 = sfs[tk[0] * T::VSFROW], s1 = sfs[tk[1] * T::VSFROW];
-        uint32_t s2 = sfs[tk[2] * T::VSFROW], s3 = sfs[tk[3] * T::VSFROW];
-        if (valid < 16) {
-          if (tk[0] >= valid) s0 = 0;
-          if (tk[1] >= valid) s1 = 0;
-          if (tk[2] >= valid) s2 = 0;
-          if (tk[3] >= valid) s3 = 0;
-        }
-        sA[bl] = e4m3x2_to_f16x2(s0 | (s1 << 8));
-        sB[bl] = e4m3x2_to_f16x2(s2 | (s3 << 8));
-      }
       // Interleave the nibbles of two tokens' bytes before converting: for
       // words W0 (token 2t) and W1 (token 2t+1), X holds in each byte the
       // even-dim code of W0 (low nibble) and of W1 (high nibble), Y the
