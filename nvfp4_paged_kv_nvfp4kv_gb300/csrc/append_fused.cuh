@@ -14,13 +14,17 @@
 
 namespace nvfp4kv {
 
+// With owners > 1 only the tokens of the unit's pages rel with
+// rel % owners == owner are handled (the pages one warp of a CTA streams).
 template <int DK, int DV>
 __device__ __forceinline__ void append_unit_tokens(const AttendParams& p, const WorkUnit& u,
-                                                   int lo, int hi, int tid, int nthreads) {
+                                                   int lo, int hi, int tid, int nthreads,
+                                                   int owner = 0, int owners = 1) {
   const int first_new = u.kv_len - u.qo_len;
   constexpr int NB = DK / 16 + DV / 16;
   for (int idx = tid; idx < (hi - lo) * NB; idx += nthreads) {
     const int tok = lo + idx / NB, blk = idx % NB, i = tok - first_new;
+    if (owners > 1 && ((tok - u.tok_begin) / 16) % owners != owner) continue;
     const bool isv = blk >= DK / 16;
     const int jb = isv ? blk - DK / 16 : blk;
     const uint16_t* src =

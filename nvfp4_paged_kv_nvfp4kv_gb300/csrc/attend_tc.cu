@@ -173,7 +173,6 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
     cp_async_commit();
   }
   int32_t next_pid = page_id(STAGES - 1);
-  if (new_lo < new_hi && !append_early) append_new();  // ordered by the barrier below
 
   // ---- Q: per-row power-of-two prescale into f16, row limits ------------
   // amax of each row (non-negative floats order like their bit patterns)
@@ -291,6 +290,14 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
 #pragma unroll
       for (int k = 0; k < 4; ++k) oacc[mt][nq][k] = 0.f;
 
+
+  // new tokens on later pages: each warp stores those of its own pages just
+  // before its loop; only this warp's later copies read them (the stores are
+  // fenced and the warp synchronised before any of them is issued)
+  if (new_lo < new_hi && !append_early) {
+    append_unit_tokens<DK, DV>(p, u, new_lo, new_hi, lane, 32, warp, WARPS);
+    __syncwarp();
+  }
 
   for (int i = 0; i < npw; ++i) {
     if (i + STAGES - 1 < npw) load_page(i + STAGES - 1, next_pid);
