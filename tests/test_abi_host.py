@@ -286,3 +286,22 @@ def test_plan_auto_kernel_choice():
                                           head_dim_qk=256, head_dim_vo=256,
                                           kv_lens=(100, 900), causal=True))
     assert plan(wide).info.kernel == 1
+
+
+def test_dequantize_rejects_bad_arguments_and_accepts_empty():
+    """nvfp4kv_dequantize_paged validates on the host before any launch."""
+    L = _lib.load()
+    s = fake_cache()
+    buf = 1 << 24
+    # nothing to do: no ids, or no output wanted
+    assert L.nvfp4kv_dequantize_paged(C.byref(s), None, 0, buf, buf, None, None) == 0
+    assert L.nvfp4kv_dequantize_paged(C.byref(s), buf, 4, None, None, None, None) == 0
+    assert L.nvfp4kv_dequantize_paged(C.byref(s), buf, -1, buf, buf, None, None) == \
+        _lib.ERR_INVALID_ARGUMENT
+    assert L.nvfp4kv_dequantize_paged(C.byref(s), None, 4, buf, buf, None, None) == \
+        _lib.ERR_INVALID_ARGUMENT
+    assert L.nvfp4kv_dequantize_paged(C.byref(s), buf, 4, buf + 4, None, None, None) == \
+        _lib.ERR_INVALID_ARGUMENT  # output not 16-byte aligned
+    bad = fake_cache(page_size=8)
+    assert L.nvfp4kv_dequantize_paged(C.byref(bad), buf, 4, buf, buf, None, None) == \
+        _lib.ERR_UNSUPPORTED
