@@ -28,10 +28,17 @@
 //    layout, so P never leaves registers.  The A operand needs pairs of
 //    tokens per dim: two converted bytes are interleaved with one byte_perm
 //    each, and multiplied by the pair of per-token scales.
+//  * With a single block of at most 8 query rows (the usual decode shape) the
+//    score product is taken transposed, S^T = K_hat . Q^T with M = 16 tokens
+//    and N = 8 rows, so that every tensor-core slot holds a real token; the
+//    two f16 P^T fragments are turned into the PV B operand with
+//    movmatrix.trans, and the row maximum is raised lazily (only when a score
+//    exceeds the running maximum by more than 2^8, decided by one warp vote
+//    per page).
 //  * Online softmax in the log2 domain; the max and sum reductions run over
-//    the 4 lanes (xor 1, 2) that hold one row.  Warps combine through shared
-//    memory; the unit writes bf16 out + lse, or an f32 partial state + lse
-//    for the merge when the plan split the request.
+//    the lanes that hold one row.  Warps combine through shared memory; the
+//    unit writes bf16 out + lse, or an f32 partial state + lse for the merge
+//    when the plan split the request.
 #include <cfloat>
 #include <cstdint>
 #include <type_traits>
