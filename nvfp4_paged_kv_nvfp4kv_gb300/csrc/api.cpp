@@ -424,8 +424,13 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
   std::vector<WorkUnit> units;
   int32_t max_units = 0;
   bool split = false;
+  int64_t n_units = 0;
   for (int b = 0; b < batch; ++b)
-    if (nq[b] > 0 && np[b] > chunk) split = true;
+    if (nq[b] > 0) {
+      if (np[b] > chunk) split = true;
+      n_units += (int64_t)num_kv_heads * ((np[b] + chunk - 1) / chunk);
+    }
+  units.reserve(static_cast<size_t>(n_units));
   int64_t partial = 0;
   std::vector<int64_t> pbase(batch, 0);
   std::vector<int32_t> nsplit(batch, 0);
@@ -455,18 +460,20 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
         units.push_back(u);
       }
   }
-  // Longest units first: when the grid takes more than one wave, the block
+  // Longest units first when the grid takes more than one wave: the block
   // scheduler then starts the long units early (longest-processing-time
-  // order); partial indices do not depend on the unit order.
-  std::stable_sort(units.begin(), units.end(), [](const WorkUnit& a, const WorkUnit& b) {
-    return a.num_pages > b.num_pages;
-  });
-  if (partial > INT32_MAX)
-    return fail(NVFP4KV_ERR_UNSUPPORTED, "too many partial states (%lld)", (long long)partial);
-  const int64_t entries = split ? (int64_t)total_rows * num_qo_heads : 0;
+  // order); partial indices do not depend on the unit order.  A grid of one
+  // wave starts every unit at once, and its order is left as built.
   int row_blocks = 0;
   for (int b = 0; b < batch; ++b)
     if (nq[b] > 0) row_blocks = std::max(row_blocks, row_blocks_of(b));
+  if ((int64_t)units.size() * row_blocks > (int64_t)num_sms * ctas_per_sm)
+    std::stable_sort(units.begin(), units.end(), [](const WorkUnit& a, const WorkUnit& b) {
+      return a.num_pages > b.num_pages;
+    });
+  if (partial > INT32_MAX)
+    return fail(NVFP4KV_ERR_UNSUPPORTED, "too many partial states (%lld)", (long long)partial);
+  const int64_t entries = split ? (int64_t)total_rows * num_qo_heads : 0;
 
   // ---- layout ------------------------------------------------------------
   const uint64_t off_flags = 0;

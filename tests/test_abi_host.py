@@ -102,7 +102,25 @@ def test_plan_covers_all_pages(name):
         assert mi[0] == 0 and mi[-1] == i.num_partials and np.all(np.diff(mi) >= 1)
     else:
         assert i.num_units == pairs
+    if ctas > i.num_sms * i.ctas_per_sm:  # more than one wave: longest units first
+        assert list(u["num_pages"]) == sorted(u["num_pages"], reverse=True)
+
+
+def test_plan_orders_multi_wave_grids_longest_first():
+    # 16-token chunks of requests of different lengths: many waves, and the
+    # last unit of each request is shorter than the rest
+    batch = W.make_batch(W.WORKLOADS["batched_decode"])
+    p = plan(batch, force_chunk_tokens=64)
+    u = check_cover(batch, p)
+    assert p.info.num_units * p.info.row_blocks > 152 * 3
+    assert len(set(u["num_pages"])) > 1
     assert list(u["num_pages"]) == sorted(u["num_pages"], reverse=True)
+    # one-wave grids keep the order they are built in: request, kv head, split
+    q = plan(batch)
+    v = units_of(q)
+    assert q.info.num_units * q.info.row_blocks <= 152 * 3
+    key = [(int(b), int(h), int(s)) for b, h, s in zip(v["b"], v["h_kv"], v["split"])]
+    assert key == sorted(key)
 
 
 def test_plan_long_context_splits_in_one_wave():
