@@ -39,6 +39,12 @@ MUTANTS = {
     "merge_unnormalised": ("double w = exp(lse_partial[i] - lse);",
                            "double w = exp(lse_partial[i] - M);"),
     "slot_from_wrong_stride": ("slot * c->v_stride_slot", "slot * c->k_stride_slot"),
+    "page_size_fixed_at_16": (
+        "  pidx = pos / c->page_size;\n",
+        "  pidx = pos / 16;\n"),
+    "kv_len_page_size_fixed_at_16": (
+        "  return (np - 1) * page_size + pt->last_page_len[b];",
+        "  return (np - 1) * 16 + pt->last_page_len[b];"),
 }
 
 

@@ -441,3 +441,42 @@ def test_append_rejects_out_of_range():
                      batch.new.k[:1], batch.new.v[:1])
     assert O.quantize_append(cache, pt, bad) == 2
     assert not cache.bufs["k_data"].any()
+
+
+@pytest.mark.parametrize("layout", ["HND", "NHD"])
+def test_page_size_one_matches_sixteen(layout):
+    """The oracle reaches every token through the page table at any page size
+    (page "Re-enable split-KV for NVFP4 KV cache in prefill path": the paged
+    layout with an indptr of pages and a last-page length): the same tokens
+    stored one per page, in permuted pages, give bit-identical float64
+    attention and the same stored bytes per token as 16-token pages."""
+    cfg = W.custom_workload(seed=11, batch=3, qo_len=2, num_qo_heads=8, num_kv_heads=2,
+                            kv_lens=(37, 100, 16), causal=True)
+    batch = W.make_batch(cfg)
+    c16, pt16 = O.cache_from_batch(batch, layout)
+    out16, lse16 = O.attention(c16, pt16, batch.qo_indptr, batch.q, cfg.num_qo_heads,
+                               True, batch.sm_scale)
+
+    lens = [int(x) for x in batch.kv_lens]
+    total = sum(lens)
+    perm = np.random.default_rng(5).permutation(total).astype(np.int32)
+    pt1 = O.PageTable(perm, np.concatenate([[0], np.cumsum(lens)]).astype(np.int32),
+                      np.ones(len(lens), np.int32))
+    lay1 = W.CacheLayout(layout, total, 1, cfg.num_kv_heads, cfg.head_dim_qk,
+                         cfg.head_dim_vo)
+    c1 = O.Cache(lay1, batch.k_global_scale, batch.v_global_scale, fill=0xFF)
+    assert O.quantize_append(c1, pt1, batch.prefix) == 0
+    assert O.quantize_append(c1, pt1, batch.new) == 0
+    out1, lse1 = O.attention(c1, pt1, batch.qo_indptr, batch.q, cfg.num_qo_heads, True,
+                             batch.sm_scale)
+    assert np.array_equal(out1, out16) and np.array_equal(lse1, lse16)
+
+    # token (b, pos) of kv head h: page perm[indptr_b + pos] slot 0 against
+    # page kv_indices[indptr16_b + pos // 16] slot pos % 16
+    kvi, kvp = batch.kv_indices.numpy(), batch.kv_indptr.numpy()
+    off = np.concatenate([[0], np.cumsum(lens)])
+    for b, pos, h in [(0, 0, 0), (0, 36, 1), (1, 17, 0), (1, 99, 1), (2, 15, 0)]:
+        for which in (0, 1):
+            a = O.dequant_row(c1, which, int(perm[off[b] + pos]), 0, h)
+            r = O.dequant_row(c16, which, int(kvi[kvp[b] + pos // 16]), pos % 16, h)
+            assert np.array_equal(a, r)
