@@ -317,18 +317,33 @@ int nvfp4kv_merge_states(const float* o_partial, const float* lse_partial,
  *           enqueued).  plan_host is the source of an asynchronous copy: keep
  *           it unchanged until the work on `stream` has completed.
  *   the other arguments are those of nvfp4kv_decode_run.
- * Each call clears the array's flag word and merge counters and copies the
- * plan's work list into it before the attention kernel, all on `stream`.
- * The first call on a device looks up the array's device address (with
- * that device current); make it before any stream capture.  All calls share
- * the one array: calls whose work overlaps on the GPU (different streams,
- * or different plans in flight at once) race and must be serialised by the
- * caller. */
+ * Every argument is checked first (as nvfp4kv_decode_run checks them, plus
+ * info->device against the current device): a call that fails enqueues
+ * nothing and leaves the array as it was.  An accepted call clears the
+ * array's flag word and merge counters and copies the plan's work list into
+ * it before the attention kernel, all on `stream`.  Outside a stream
+ * capture every call looks up the array's device address on the current
+ * device; inside a capture the address found by that device's last
+ * uncaptured call is used, so make one call before capturing (otherwise
+ * INVALID_ARGUMENT).  All calls share the one array: calls whose work
+ * overlaps on the GPU (different streams, or different plans in flight at
+ * once) race and must be serialised by the caller.  A bad page id sets
+ * NVFP4KV_FLAG_BAD_PAGE_INDEX in the array's flag word: read it with
+ * nvfp4kv_static_workspace_flags before the next call clears it. */
 int nvfp4kv_decode_run_static(const nvfp4kv_plan_info* info, const void* plan_host,
                               const void* q_bf16, int64_t q_stride_tok,
                               int64_t q_stride_head, const nvfp4kv_paged_cache* cache,
                               const int32_t* kv_indices, float sm_scale,
                               void* out_bf16, float* lse, cudaStream_t stream);
+
+/* The device flag word of the static workspace (the flags of the last
+ * nvfp4kv_decode_run_static call on the current device), read as
+ * nvfp4kv_workspace_flags reads a caller workspace: synchronises `stream`,
+ * optionally clears the word, and returns NVFP4KV_ERR_DEVICE_CHECK when a
+ * flag is set (*flags is written either way).  info is the plan of that
+ * call.  No counterpart on the pages, like the entry point it serves. */
+int nvfp4kv_static_workspace_flags(const nvfp4kv_plan_info* info, uint32_t* flags,
+                                   int32_t clear, cudaStream_t stream);
 
 /* ---- flags ---------------------------------------------------------------- */
 /* Read (and optionally clear) the device flag word of a planned workspace.

@@ -7,4 +7,5 @@ from .api import (NvFp4KvError, PagedCache, Plan, default_sm_scale,  # noqa: F40
                   nvfp4kv_decode_attend, nvfp4kv_decode_merge, nvfp4kv_decode_plan,
                   nvfp4kv_decode_run, nvfp4kv_merge_states, nvfp4kv_quantize_append,
                   nvfp4kv_workspace_flags, nvfp4kv_decode_run_static,
+                  nvfp4kv_static_workspace_flags,
                   nvfp4kv_decode_append_run, nvfp4kv_dequantize_paged)

@@ -84,6 +84,8 @@ SIGNATURES = {
     "nvfp4kv_merge_states": (C.c_int, [_vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp]),
     "nvfp4kv_workspace_flags": (C.c_int, [C.POINTER(PlanInfo), _vp, C.POINTER(C.c_uint32),
                                           _i32, _vp]),
+    "nvfp4kv_static_workspace_flags": (C.c_int, [C.POINTER(PlanInfo),
+                                                 C.POINTER(C.c_uint32), _i32, _vp]),
     "nvfp4kv_decode_run_static": (C.c_int, [
         C.POINTER(PlanInfo), _vp, _vp, _i64, _i64, C.POINTER(PagedCacheStruct), _vp, _f32,
         _vp, _vp, _vp]),

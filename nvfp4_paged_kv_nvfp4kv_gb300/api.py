@@ -18,7 +18,8 @@ from ._lib import NvFp4KvError, PagedCacheStruct, PlanInfo, PlanOptions, check
 __all__ = ["PagedCache", "Plan", "NvFp4KvError", "nvfp4kv_quantize_append",
            "nvfp4kv_decode_plan", "nvfp4kv_decode_run", "nvfp4kv_decode_attend",
            "nvfp4kv_decode_merge", "nvfp4kv_merge_states", "nvfp4kv_workspace_flags",
-           "nvfp4kv_decode_run_static", "nvfp4kv_decode_append_run",
+           "nvfp4kv_decode_run_static", "nvfp4kv_static_workspace_flags",
+           "nvfp4kv_decode_append_run",
            "nvfp4kv_dequantize_paged"]
 
 
@@ -294,3 +295,13 @@ def nvfp4kv_decode_run_static(plan: Plan, q: torch.Tensor, cache: PagedCache, kv
 
 def default_sm_scale(head_dim_qk: int) -> float:
     return 1.0 / math.sqrt(head_dim_qk)
+
+
+def nvfp4kv_static_workspace_flags(plan: Plan, clear: bool = False, stream=None) -> int:
+    """The flag word of the static workspace after nvfp4kv_decode_run_static."""
+    flags = C.c_uint32(0)
+    st = _lib.load().nvfp4kv_static_workspace_flags(C.byref(plan.info), C.byref(flags),
+                                                    int(clear), _stream(stream))
+    if st not in (_lib.OK, _lib.ERR_DEVICE_CHECK):
+        check(st, "nvfp4kv_static_workspace_flags")
+    return int(flags.value)

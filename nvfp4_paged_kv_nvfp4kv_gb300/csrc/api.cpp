@@ -565,6 +565,14 @@ int check_run(const nvfp4kv_plan_info* info, const void* q, int64_t qst, int64_t
   if (!workspace || workspace_bytes < info->workspace_bytes || !aligned(workspace, 256))
     return fail(NVFP4KV_ERR_WORKSPACE_TOO_SMALL, "workspace needs %llu bytes, 256-aligned",
                 (unsigned long long)info->workspace_bytes);
+  if (info->device >= 0) {  // the plan's SM count, occupancy and smem sizing
+    int cur = -1;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (cur != info->device)
+      return fail(NVFP4KV_ERR_PLAN_MISMATCH, "plan made for device %d, current device is %d",
+                  info->device, cur);
+  }
   if (info->num_units == 0) return NVFP4KV_OK;
   if (!q || !kv_indices || !out)
     return fail(NVFP4KV_ERR_INVALID_ARGUMENT, "null q / kv_indices / out");
@@ -576,9 +584,15 @@ int check_run(const nvfp4kv_plan_info* info, const void* q, int64_t qst, int64_t
 
 }  // namespace
 
-extern "C" {
-
-}  // extern "C"
+namespace nvfp4kv {
+// The argument checks of nvfp4kv_decode_run, for entry points that must
+// validate before they enqueue anything of their own.
+int validate_run(const nvfp4kv_plan_info* info, const void* q, int64_t qst, int64_t qsh,
+                 const nvfp4kv_paged_cache* cache, const int32_t* kv_indices,
+                 const void* workspace, uint64_t workspace_bytes, const void* out) {
+  return check_run(info, q, qst, qsh, cache, kv_indices, workspace, workspace_bytes, out);
+}
+}  // namespace nvfp4kv
 
 namespace {
 

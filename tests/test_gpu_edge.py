@@ -255,3 +255,38 @@ def test_dequantize_paged_bad_page_and_partial_outputs():
     assert int(g.flags.item()) & N._lib.FLAG_BAD_PAGE_INDEX
     assert bool((k[1:] == 0).all())
     assert bool((k[0].abs().sum() > 0))
+
+
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_q_rows_wider_than_f16_range(kernel):
+    """Q rows whose dynamic range exceeds f16's (about 40 binades).  The
+    tensor-core kernel scales each bf16 Q row by a power of two so its
+    largest entry lands near 2^14 and converts it to f16: entries more than
+    ~2^-38 below the row maximum become f16 subnormals or zero.  Their share
+    of a score is below 2^-30 of it, so the results must stay within the
+    usual tolerance of the float64 oracle (which keeps every entry): rows of
+    tiny values only (2^-100 and 2^-14 times N(0,1)), a 2^6 outlier beside
+    entries of 2^-30, and N(0,1) rows with a quarter of the entries at 2^-24
+    and a quarter at 2^-60 of their size (60 binades)."""
+    batch = small(kv_lens=(37, 100, 250, 1000), num_qo_heads=8, num_kv_heads=2)
+    q = batch.q.float()
+    gen = torch.Generator().manual_seed(9)
+    rows, heads, d = q.shape
+    for r in range(rows):
+        for h in range(heads):
+            kind = (r * heads + h) % 5
+            if kind == 0:                     # every entry tiny
+                q[r, h] *= 2.0 ** -100
+            elif kind == 1:                   # every entry small
+                q[r, h] *= 2.0 ** -14
+            elif kind == 2:                   # one outlier, the rest tiny
+                q[r, h] *= 2.0 ** -30
+                q[r, h, int(torch.randint(0, d, (1,), generator=gen))] = 64.0
+            elif kind == 3:                   # N(0,1) with entries 2^-24 and 2^-60
+                idx = torch.randperm(d, generator=gen)
+                q[r, h, idx[: d // 4]] *= 2.0 ** -24
+                q[r, h, idx[d // 4: d // 2]] *= 2.0 ** -60
+            # kind 4: untouched N(0,1)
+    batch.q = q.to(torch.bfloat16)
+    stats, g, (out, lse) = check(batch, kernel=kernel, force_chunk_tokens=64)
+    assert bool(torch.isfinite(out.float()).all()) and bool(torch.isfinite(lse).all())

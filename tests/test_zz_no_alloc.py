@@ -65,3 +65,46 @@ def test_static_workspace_rejects_plans_beyond_its_size():
     assert "16 MiB" in err.value.detail
     torch.cuda.synchronize()
     assert torch.all(out.float() == 7.0)   # nothing ran
+
+
+def test_static_workspace_reports_a_bad_page_id():
+    """A page id outside the pool sets the bad-page flag in the static
+    array's flag word; nvfp4kv_static_workspace_flags reads it (and clears
+    it), and the next good call reports a clean word."""
+    batch = W.make_batch(W.custom_workload(seed=33, batch=2, kv_lens=(37, 300),
+                                           num_qo_heads=8, num_kv_heads=2))
+    g = H.GpuCase(batch)
+    plan = host_plan(batch)
+    rows, c = int(batch.qo_indptr[-1]), batch.cfg
+    out = torch.empty((rows, c.num_qo_heads, c.head_dim_vo), dtype=torch.bfloat16,
+                      device="cuda")
+    bad = g.kv_indices.clone()
+    bad[2] = batch.num_pages + 11
+    N.nvfp4kv_decode_run_static(plan, g.q, g.cache, bad, batch.sm_scale, out=out)
+    assert N.nvfp4kv_static_workspace_flags(plan, clear=True) & _lib.FLAG_BAD_PAGE_INDEX
+    assert N.nvfp4kv_static_workspace_flags(plan) == 0
+    N.nvfp4kv_decode_run_static(plan, g.q, g.cache, g.kv_indices, batch.sm_scale, out=out)
+    assert N.nvfp4kv_static_workspace_flags(plan) == 0
+    assert bool(torch.isfinite(out.float()).all())
+
+
+def test_static_workspace_rejected_call_leaves_the_array_alone():
+    """A call that fails argument checks enqueues nothing: the flag word the
+    previous call left is still there."""
+    batch = W.make_batch(W.custom_workload(seed=34, batch=2, kv_lens=(40, 90),
+                                           num_qo_heads=4, num_kv_heads=1))
+    g = H.GpuCase(batch)
+    plan = host_plan(batch)
+    bad = g.kv_indices.clone()
+    bad[0] = -3
+    out = torch.empty((2, 4, 128), dtype=torch.bfloat16, device="cuda")
+    N.nvfp4kv_decode_run_static(plan, g.q, g.cache, bad, batch.sm_scale, out=out)
+    torch.cuda.synchronize()
+    n = g.q.numel()
+    q_off = torch.empty(n + 8, dtype=torch.bfloat16, device="cuda")[1:1 + n].view(g.q.shape)
+    q_off.copy_(g.q)
+    with pytest.raises(N.NvFp4KvError) as err:   # q misaligned: rejected on the host
+        N.nvfp4kv_decode_run_static(plan, q_off, g.cache, g.kv_indices, batch.sm_scale,
+                                    out=out)
+    assert err.value.status == _lib.ERR_INVALID_ARGUMENT
+    assert N.nvfp4kv_static_workspace_flags(plan, clear=True) & _lib.FLAG_BAD_PAGE_INDEX
