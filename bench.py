@@ -218,6 +218,8 @@ def run_gpu(args, world, rank, local):
     out = torch.empty((rows, c.num_qo_heads, c.head_dim_vo), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((rows, c.num_qo_heads), dtype=torch.float32, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush_r = (torch.zeros(512 << 20, dtype=torch.uint8, device=dev)
+               if args.l2_flush == "write_read" else None)
     stream = torch.cuda.current_stream(dev)
 
     # the step's new tokens, row-aligned with the query rows
@@ -242,9 +244,14 @@ def run_gpu(args, world, rank, local):
             ev[2].record(stream)
 
     def pre_step():
-        flush.fill_(1)              # evict the cache (> L2) between steps
+        l2_flush()
         torch.cuda._sleep(200000)   # bounded spin: keep the GPU busy while the
         #                             host enqueues the step back to back
+
+    def l2_flush():
+        flush.fill_(1)              # evict the cache (write > L2) between steps
+        if flush_r is not None:     # then read > L2: the flush's dirty lines are
+            flush_r.max()           # written back here, not inside the timed step
 
     for _ in range(args.warmup):
         pre_step()
@@ -303,7 +310,7 @@ def run_gpu(args, world, rank, local):
     d2h = h_res.numel()
     times = []
     for k in range(e2e_steps + 3):
-        flush.fill_(1)
+        l2_flush()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         d_in.copy_(h_in, non_blocking=True)
@@ -344,7 +351,10 @@ def run_gpu(args, world, rank, local):
             "step": ("quantize_append + decode_run (two launches)" if args.separate_append else
                      "decode_append_run: new tokens quantised into their pages, attention and "
                      "split-KV merge in one launch") + "; plan built once",
-            "l2": "flushed between steps (512 MB write)",
+            "l2": ("flushed between steps: 512 MB write, then 512 MB read (no dirty "
+                   "lines of the flush are written back inside the timed step)"
+                   if args.l2_flush == "write_read" else
+                   "flushed between steps (512 MB write)"),
             "kernel": {1: "tensor-core mma.sync f16/f32acc",
                        2: "CUDA-core f32",
                        3: "tcgen05.mma f16/f32acc, K_hat in tensor memory"}[plan.info.kernel],
@@ -501,6 +511,9 @@ def main():
     ap.add_argument("--chunk-tokens", type=int, default=0,
                     help="split-KV chunk in tokens (multiple of 16); 0 = the planner's choice")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--l2-flush", default="write", choices=["write", "write_read"],
+                    help="between steps: write 512 MB (default), or write 512 MB and then "
+                         "read another 512 MB so no dirty lines are left in L2")
     ap.add_argument("--separate-append", action="store_true",
                     help="quantize_append and decode_run as two launches per step")
     args = ap.parse_args()

@@ -21,6 +21,7 @@ namespace nvfp4kv {
 bool attend_config_tc(int dk, int dv, int rows, AttendConfig* cfg);
 bool attend_config_simt(int dk, int dv, int rows, AttendConfig* cfg);
 bool attend_config_tcgen05(int dk, int dv, int rows, AttendConfig* cfg);
+bool attend_config_dec(int dk, int dv, int rows, AttendConfig* cfg);
 cudaError_t prepare_kernel(const AttendConfig& cfg);
 }  // namespace nvfp4kv
 
@@ -144,6 +145,21 @@ bool lookup_kernel(int kind, int dk, int dv, int rows, AttendConfig* cfg) {
 }
 
 constexpr int kMinChunkPages = 8;
+
+// The bulk-copy decode kernel reads each (page, head) region of the four
+// buffers with one copy: the 16 slots' rows must be contiguous, every region
+// must start 16-byte aligned, and a page offset must fit 32 bits.
+bool bulk_decode_layout(const nvfp4kv_paged_cache* c) {
+  const int64_t kr = c->head_dim_qk / 2, vr = c->head_dim_vo / 2;
+  const int64_t ksr = c->head_dim_qk / 16, vsr = c->head_dim_vo / 16;
+  const int64_t lim = (int64_t)1 << 32;
+  return c->k_stride_slot == kr && c->v_stride_slot == vr && c->k_sf_stride_slot == ksr &&
+         c->v_sf_stride_slot == vsr && aligned(c->k_sf, 16) && aligned(c->v_sf, 16) &&
+         c->k_sf_stride_page % 16 == 0 && c->k_sf_stride_head % 16 == 0 &&
+         c->v_sf_stride_page % 16 == 0 && c->v_sf_stride_head % 16 == 0 &&
+         c->k_stride_page < lim && c->v_stride_page < lim && c->k_sf_stride_page < lim &&
+         c->v_sf_stride_page < lim;
+}
 
 }  // namespace
 
@@ -622,8 +638,14 @@ int attend(const nvfp4kv_plan_info* info, const void* q_bf16, int64_t q_stride_t
   }
   if (info->num_units == 0) return ok();
   AttendConfig cfg{};
-  if (!lookup_kernel(info->kernel, info->head_dim_qk, info->head_dim_vo, info->rows_per_block,
-                     &cfg))
+  // a tensor-core plan of one block of <= 8 rows runs the bulk-copy decode
+  // kernel when the cache layout allows it (same arithmetic, same occupancy
+  // or better: the plan's one-wave grid stays one wave)
+  const bool dec = info->kernel == kKernelTensorCore && info->rows_per_block == 8 &&
+                   bulk_decode_layout(cache) &&
+                   attend_config_dec(info->head_dim_qk, info->head_dim_vo, 8, &cfg);
+  if (!dec && !lookup_kernel(info->kernel, info->head_dim_qk, info->head_dim_vo,
+                             info->rows_per_block, &cfg))
     return fail(NVFP4KV_ERR_UNSUPPORTED, "planned kernel not available");
   cudaError_t e = prepare_kernel(cfg);
   if (e != cudaSuccess) return cuda_fail(e, "kernel attributes");

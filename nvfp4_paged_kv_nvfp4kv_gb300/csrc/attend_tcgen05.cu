@@ -807,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
         }
       }
       if (partial)
-        merge_if_last<N, DV, 256>(p, u, row0, R, s_fin, tid, [] { named_sync(3, 256); });
+        merge_if_last<N, DV, 256, 4>(p, u, row0, R, s_fin, tid, [] { named_sync(3, 256); });
     }
     tc_fence_before();
   }

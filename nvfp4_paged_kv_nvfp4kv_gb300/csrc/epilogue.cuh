@@ -20,12 +20,16 @@ namespace nvfp4kv {
 // The split group's last CTA folds its partials.  Run by NTHREADS threads
 // (tid in [0, NTHREADS)) that synchronise with `sync`; sFin: scratch of at
 // least RB floats + 1 int.  Every thread must have stored its partials.
-template <int RB, int DV, int NTHREADS, class Sync>
+// Each thread folds whole (row, 4 dims) items: batches of MB partial states
+// (their lse and o loaded together) with a running maximum, so the fold
+// costs ceil(S / MB) dependent L2 round trips.
+template <int RB, int DV, int NTHREADS, int MB = 8, class Sync>
 __device__ __forceinline__ void merge_if_last(const AttendParams& p, const WorkUnit& u,
                                               int row0, int R, float* sFin, int tid,
                                               Sync sync) {
   using namespace dev;
   constexpr float kLog2e = 1.44269504088896340736f;
+  constexpr float kLn2 = 0.69314718055994530942f;
   const int G = p.group, Hq = p.num_qo_heads;
   int* s_last = reinterpret_cast<int*>(sFin + 2 * RB);
   __threadfence();
@@ -40,59 +44,51 @@ __device__ __forceinline__ void merge_if_last(const AttendParams& p, const WorkU
   if (!*s_last) return;
   __threadfence();
   const int S = u.num_splits;
-  const int lane = tid & 31, warp = tid >> 5;
-  // per row: M = max lse_s, Lf = M + ln sum exp(lse_s - M)  (natural log)
-  for (int rr = warp; rr < RB; rr += NTHREADS / 32) {
-    const int r = row0 + rr;
-    if (r >= R) continue;
-    const int i = r / G, head = u.h_kv * G + r % G;
-    const float* lp = p.partial_lse + (int64_t)u.partial_base +
-                      ((int64_t)i * Hq + head) * S;
-    float M = -INFINITY;
-    for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldcg(lp + s));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float sum = 0.f;
-    if (M != -INFINITY)
-      for (int s = lane; s < S; s += 32) sum += ex2((__ldcg(lp + s) - M) * kLog2e);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane == 0) sFin[rr] = (M == -INFINITY) ? -INFINITY : M + logf(sum);
-  }
-  sync();
-  for (int idx = tid; idx < RB * (DV / 2); idx += NTHREADS) {
-    const int rr = idx / (DV / 2), d = 2 * (idx % (DV / 2));
-    const int r = row0 + rr;
+  constexpr int DQ = DV / 4;
+  for (int idx = tid; idx < RB * DQ; idx += NTHREADS) {
+    const int rr = idx / DQ, d4 = idx % DQ, r = row0 + rr;
     if (r >= R) continue;
     const int i = r / G, head = u.h_kv * G + r % G;
     const int64_t base = (int64_t)u.partial_base + ((int64_t)i * Hq + head) * S;
-    const float Lf = sFin[rr];
-    float o0 = 0.f, o1 = 0.f;
-    if (Lf != -INFINITY) {
-      // batches of 16 partials: all loads of a batch are in flight together
-      for (int s0 = 0; s0 < S; s0 += 16) {
-        float lw[16];
-        float2 v[16];
+    float M = -INFINITY, L = 0.f;  // running max (log2 units) and sum
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < S; s0 += MB) {
+      float lw[MB];
+      float4 v[MB];
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (s0 + j < S) {
-            lw[j] = __ldcg(p.partial_lse + base + s0 + j);
-            v[j] = __ldcg(reinterpret_cast<const float2*>(p.partial_o + (base + s0 + j) * DV + d));
-          }
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (s0 + j < S) {
-            const float w = ex2((lw[j] - Lf) * kLog2e);
-            o0 += w * v[j].x;
-            o1 += w * v[j].y;
-          }
+      for (int j = 0; j < MB; ++j) {
+        lw[j] = -INFINITY;
+        v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (s0 + j < S) {
+          lw[j] = __ldcg(p.partial_lse + base + s0 + j) * kLog2e;
+          v[j] = __ldcg(reinterpret_cast<const float4*>(p.partial_o + (base + s0 + j) * DV) + d4);
+        }
       }
+      float mb = lw[0];
+#pragma unroll
+      for (int j = 1; j < MB; ++j) mb = fmaxf(mb, lw[j]);
+      if (mb == -INFINITY) continue;
+      const float mn = fmaxf(M, mb);
+      const float cf = M == -INFINITY ? 0.f : ex2(M - mn);
+      L *= cf;
+      acc.x *= cf; acc.y *= cf; acc.z *= cf; acc.w *= cf;
+#pragma unroll
+      for (int j = 0; j < MB; ++j) {
+        const float w = ex2(lw[j] - mn);  // 0 for lw = -inf
+        L += w;
+        acc.x += w * v[j].x; acc.y += w * v[j].y; acc.z += w * v[j].z; acc.w += w * v[j].w;
+      }
+      M = mn;
     }
+    const bool any = M != -INFINITY && L > 0.f;
+    const float inv = any ? 1.f / L : 0.f;
     const int64_t qrow = u.qo_begin + i;
-    const uint32_t packed =
-        (uint32_t)f32_to_bf16_bits(o0) | ((uint32_t)f32_to_bf16_bits(o1) << 16);
-    *reinterpret_cast<uint32_t*>(p.out + (qrow * Hq + head) * DV + d) = packed;
-    if (d == 0 && p.lse) p.lse[qrow * Hq + head] = Lf;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(p.out + (qrow * Hq + head) * DV + 4 * d4);
+    dst[0] = (uint32_t)f32_to_bf16_bits(acc.x * inv) |
+             ((uint32_t)f32_to_bf16_bits(acc.y * inv) << 16);
+    dst[1] = (uint32_t)f32_to_bf16_bits(acc.z * inv) |
+             ((uint32_t)f32_to_bf16_bits(acc.w * inv) << 16);
+    if (d4 == 0 && p.lse) p.lse[qrow * Hq + head] = any ? (M + log2f(L)) * kLn2 : -INFINITY;
   }
 }
 
@@ -149,7 +145,7 @@ __device__ __forceinline__ void finish_unit(const AttendParams& p, const WorkUni
   }
   if (!partial) return;
 
-  merge_if_last<RB, DV, WARPS * 32>(p, u, row0, R, sFin, tid, [] { __syncthreads(); });
+  merge_if_last<RB, DV, WARPS * 32, 16>(p, u, row0, R, sFin, tid, [] { __syncthreads(); });
 }
 
 }  // namespace nvfp4kv
