@@ -38,8 +38,9 @@ UNIT = "KV tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attend_tc_long_context_decode.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "nvfp4_paged_kv_nvfp4kv_gb300", "csrc", f)
-                  for f in ("attend_tc.cu", "append_fused.cuh", "device_common.cuh",
-                            "epilogue.cuh", "internal.h", "quantize.cuh", "stage.cuh")]
+                  for f in ("attend_dec.cu", "attend_tc.cu", "append_fused.cuh",
+                            "device_common.cuh", "epilogue.cuh", "internal.h", "quantize.cuh",
+                            "stage.cuh")]
 
 
 def workload_desc(cfg: W.Workload) -> str:
@@ -274,14 +275,21 @@ def run_gpu(args, world, rank, local):
     else:  # one launch: no event between append and attention
         t_append, t_attend = [0.0], t_step
     ms_step = statistics.mean(t_step)
+    q = sorted(t_step)
+    spread = {"median": statistics.median(q), "p10": q[len(q) // 10],
+              "p90": q[(9 * len(q)) // 10], "min": q[0], "max": q[-1]}
     ms_step_max = max_over_ranks(ms_step, world)
     kv_tokens = sum(batch.kv_lens)
     value = kv_tokens * world / (ms_step_max * 1e-3)
 
     # ---- end to end through the public API with host buffers -------------
-    # The step's inputs travel in one pinned host buffer and one copy; the
-    # library reads them through 16-byte-aligned slices of one device buffer
-    # (out and lse come back the same way).
+    # Serving makes a plan once per change of the batch's page or query
+    # counts: here one plan with live last-page lengths (plan option
+    # device_last_page_len).  Every step copies its inputs (Q, the new tokens'
+    # K/V, the requests' last page lengths) from one pinned host buffer, runs
+    # the fused append + attention, and copies out and lse back.  The step's
+    # three calls are captured once as a CUDA graph and replayed; the eager
+    # figure issues them every step.
     def packed(tensors, device):
         offs, n = [], 0
         for t in tensors:
@@ -292,45 +300,62 @@ def run_gpu(args, world, rank, local):
         views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
                  for o, t in zip(offs, tensors)]
         return buf, views
-    src = [batch.q, batch.new.k[order].contiguous(), batch.new.v[order].contiguous()]
+    src = [batch.q, batch.new.k[order].contiguous(), batch.new.v[order].contiguous(),
+           batch.last_page_len.to(torch.int32).contiguous()]
     if args.separate_append:  # the two-launch step also needs request and position
         src += [batch.new.batch_idx[order].contiguous(), batch.new.positions[order].contiguous()]
     h_in, h_views = packed(src, "cpu")
     for hv, t in zip(h_views, src):
         hv.copy_(t)
     d_in, d_views = packed(src, dev)
-    d_q, d_k, d_v = d_views[:3]
-    d_b, d_p = (d_views[3], d_views[4]) if args.separate_append else (None, None)
+    d_q, d_k, d_v, d_lpl = d_views[:4]
+    d_b, d_p = (d_views[4], d_views[5]) if args.separate_append else (None, None)
     h_res, (h_out, h_lse) = packed([out, lse], "cpu")
     d_res, (e_out, e_lse) = packed([out, lse], dev)
-    e2e_steps = max(3, min(args.steps, 200))
-    # bytes moved per step: the packed buffers (with their alignment padding)
-    # and the plan's work list
-    h2d = h_in.numel() + int(plan.info.plan_host_bytes)
-    d2h = h_res.numel()
-    times = []
-    for k in range(e2e_steps + 3):
-        l2_flush()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        d_in.copy_(h_in, non_blocking=True)
-        p2 = N.nvfp4kv_decode_plan(batch.qo_indptr, batch.kv_indptr, batch.last_page_len,
+    d_in.copy_(h_in)
+    plan_e = N.nvfp4kv_decode_plan(batch.qo_indptr, batch.kv_indptr, batch.last_page_len,
                                    c.num_qo_heads, c.num_kv_heads, c.head_dim_qk,
                                    c.head_dim_vo, causal=c.causal, kernel=args.kernel,
-                                   force_chunk_tokens=args.chunk_tokens,
-                                   device=local, reuse=plan)
+                                   force_chunk_tokens=args.chunk_tokens, device=local,
+                                   device_last_page_len=d_lpl)
+
+    def e2e_step():
+        d_in.copy_(h_in, non_blocking=True)
         if args.separate_append:
-            N.nvfp4kv_quantize_append(cache, d_k, d_v, d_b, d_p, kv_indices, kv_indptr, last,
+            N.nvfp4kv_quantize_append(cache, d_k, d_v, d_b, d_p, kv_indices, kv_indptr, d_lpl,
                                       device_flags=flags)
-            N.nvfp4kv_decode_run(p2, d_q, cache, kv_indices, batch.sm_scale, out=e_out,
+            N.nvfp4kv_decode_run(plan_e, d_q, cache, kv_indices, batch.sm_scale, out=e_out,
                                  lse=e_lse)
         else:
-            N.nvfp4kv_decode_append_run(p2, d_k, d_v, d_q, cache, kv_indices, batch.sm_scale,
-                                        out=e_out, lse=e_lse)
+            N.nvfp4kv_decode_append_run(plan_e, d_k, d_v, d_q, cache, kv_indices,
+                                        batch.sm_scale, out=e_out, lse=e_lse)
         h_res.copy_(d_res, non_blocking=True)
-        stream.synchronize()
-        if k >= 3:
-            times.append(time.perf_counter() - t0)
+
+    e2e_step()  # eager first call (the library prepares the kernel once)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 200))
+    # bytes moved per step: the packed buffers, with their alignment padding
+    h2d = h_in.numel()
+    d2h = h_res.numel()
+
+    def time_e2e(run):
+        ts = []
+        for k in range(e2e_steps + 3):
+            l2_flush()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            run()
+            torch.cuda.synchronize()
+            if k >= 3:
+                ts.append(time.perf_counter() - t0)
+        return ts
+    times = time_e2e(graph.replay)
+    assert torch.equal(h_out.view(torch.int16), out.cpu().view(torch.int16))
+    times_eager = time_e2e(e2e_step)
     assert torch.equal(h_out.view(torch.int16), out.cpu().view(torch.int16))
     e2e_s = max_over_ranks(statistics.mean(times), world)
     e2e_value = kv_tokens * world / e2e_s
@@ -345,7 +370,7 @@ def run_gpu(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic",
+        "dtype": "f16 operands (exact e2m1 x E4M3), f32 accumulate", "data": "synthetic",
         "config": {
             "workload": workload_desc(cfg), "layout": args.layout,
             "step": ("quantize_append + decode_run (two launches)" if args.separate_append else
@@ -361,6 +386,7 @@ def run_gpu(args, world, rank, local):
             "split_units": int(plan.info.num_units), "split": int(plan.info.split),
             "chunk_pages": int(plan.info.chunk_pages),
             "us_per_call": ms_step_max * 1e3,
+            "us_per_call_spread": {k: v * 1e3 for k, v in spread.items()},
             "us_attend_incl_fused_merge": ms_attend * 1e3,
             "us_separate_append": (statistics.mean(t_append) * 1e3
                                    if args.separate_append else None),
@@ -372,7 +398,13 @@ def run_gpu(args, world, rank, local):
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": peak_kind},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
+                "ms_per_step_median": statistics.median(times) * 1e3,
+                "ms_per_step_eager": statistics.mean(times_eager) * 1e3,
+                "how": "plan with live last-page lengths made once; per step: inputs "
+                       "copied from one pinned host buffer, fused append + attention, out "
+                       "and lse copied back; the three calls replayed as a CUDA graph "
+                       "(ms_per_step_eager: issued eagerly)"},
         "gpu_launches": args.steps * (2 if args.separate_append else 1),
         "clocks": clk.summary(),
     }
@@ -425,52 +457,84 @@ def _oracle_units(O, cache, pt, batch, units, threads, chunk=None):
     return out, lse
 
 
-def cpu_baseline(batch, layout, min_s: float = 10.0, max_passes: int = 100):
-    """The oracle as it stands on the host cores: up to 4 requests of the
-    workload, one (request, kv head) unit per thread, whole passes repeated
-    until about ``min_s`` seconds of CPU work (at most ``max_passes``)."""
-    O = _oracle()
-    c = batch.cfg
-    requests = list(range(min(4, c.batch)))
-    cache, pt = _oracle_prefix_cache(batch, requests, layout)
-    units = [(b, h) for b in requests for h in range(c.num_kv_heads)]
-    threads = min(len(units), os.cpu_count() or 1)
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model", "hardware")):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+def _timed_passes(O, cache, pt, batch, units, threads, min_s, max_passes):
     passes, t0 = 0, time.perf_counter()
     while True:
         _oracle_units(O, cache, pt, batch, units, threads)
         passes += 1
         dt = time.perf_counter() - t0
         if dt >= min_s or passes >= max_passes:
-            break
+            return passes, dt
+
+
+def cpu_baseline(batch, layout, min_s: float = 10.0, max_passes: int = 100):
+    """The oracle as it stands on the host cores: up to 4 requests of the
+    workload, one (request, kv head) unit per thread on all cores (whole
+    passes repeated for about ``min_s`` seconds, at most ``max_passes``), and
+    the same oracle on one core over the first request's first kv head."""
+    O = _oracle()
+    c = batch.cfg
+    cores = os.cpu_count() or 1
+    requests = list(range(min(4, c.batch)))
+    cache, pt = _oracle_prefix_cache(batch, requests, layout)
+    units = [(b, h) for b in requests for h in range(c.num_kv_heads)]
+    threads = min(len(units), cores)
+    passes, dt = _timed_passes(O, cache, pt, batch, units, threads, min_s, max_passes)
     toks = sum(batch.kv_lens[b] for b in requests)
+    p1, dt1 = _timed_passes(O, cache, pt, batch, [(0, 0)], 1, min_s / 3, max_passes)
     return {"value": toks * passes / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "cpu_count": cores, "cpu_model": cpu_model(),
+            "value_1core": batch.kv_lens[0] / c.num_kv_heads * p1 / dt1,
             "sample": "requests %s of the workload (%d KV tokens x %d kv heads), append of "
-                      "their new tokens + float64 exact attention, %d passes in %.1f s" % (
-                          requests, toks, c.num_kv_heads, passes, dt)}
+                      "their new tokens + float64 exact attention, one (request, kv head) "
+                      "unit per thread on %d threads, %d passes in %.1f s; value_1core: "
+                      "request 0, kv head 0 on one thread, %d passes in %.1f s" % (
+                          requests, toks, c.num_kv_heads, threads, passes, dt, p1, dt1)}
 
 
 def run_reference(args, world, rank):
-    """The oracle timed on the host cores: each step appends one request's new
-    token and runs exact attention for a bounded slice of its kv heads."""
+    """The oracle timed on the host cores: each step appends the new tokens of
+    a bounded sample of (request, kv head) units and runs exact attention for
+    them, one unit per thread on all cores."""
     if rank != 0:
         return None
     O = _oracle()
     cfg = W.WORKLOADS[args.workload]
     batch = W.make_batch(cfg)
-    req = 0
-    cache, pt = _oracle_prefix_cache(batch, [req], args.layout)
-    # Per-step sample: as many kv heads of the request as fit the time budget
-    # of the whole --warmup + --steps run (NVFP4KV_REF_BUDGET_S, default 150 s);
-    # if even one head per step is slower, the run stops at the budget and
-    # reports the steps it timed.
+    cores = os.cpu_count() or 1
+    requests = list(range(min(4, cfg.batch)))
+    cache, pt = _oracle_prefix_cache(batch, requests, args.layout)
+    all_units = [(b, h) for b in requests for h in range(cfg.num_kv_heads)]
+    # Per-step sample: as many units as fit the time budget of the whole
+    # --warmup + --steps run (NVFP4KV_REF_BUDGET_S, default 150 s), at least
+    # one; if even one unit per step is slower, the run stops at the budget
+    # and reports the steps it timed.
     budget = float(os.environ.get("NVFP4KV_REF_BUDGET_S", "150"))
     t0 = time.perf_counter()
-    _oracle_units(O, cache, pt, batch, [(req, 0)], 1)
+    _oracle_units(O, cache, pt, batch, all_units[:1], 1)
     unit_s = time.perf_counter() - t0
     per_step = budget / max(1, args.steps + args.warmup)
-    heads = max(1, min(cfg.num_kv_heads, int(per_step / max(unit_s, 1e-9))))
-    threads = min(heads, os.cpu_count() or 1)
-    units = [(req, h) for h in range(heads)]
+    n_units = max(1, min(len(all_units), int(per_step / max(unit_s, 1e-9) * cores)))
+    units = all_units[:n_units]
+    threads = min(n_units, cores)
     times = []
     start = time.perf_counter()
     for k in range(args.warmup + args.steps):
@@ -481,7 +545,7 @@ def run_reference(args, world, rank):
         if len(times) >= 3 and time.perf_counter() - start > budget:
             break
     dt = statistics.mean(times)
-    toks = batch.kv_lens[req] * heads / cfg.num_kv_heads
+    toks = sum(batch.kv_lens[b] for b, _ in units) / cfg.num_kv_heads
     value = toks / dt
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -489,11 +553,11 @@ def run_reference(args, world, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": workload_desc(cfg), "layout": args.layout,
-                   "sample": "request %d, %d of %d kv heads per step" % (
-                       req, heads, cfg.num_kv_heads)},
+                   "sample": "%d (request, kv head) units per step" % n_units},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": "request %d (%d KV tokens), %d kv heads per step" % (
-                             req, batch.kv_lens[req], heads)},
+                         "cpu_count": cores, "cpu_model": cpu_model(),
+                         "sample": "%d (request, kv head) units of requests %s per step, one "
+                                   "per thread" % (n_units, sorted({b for b, _ in units}))},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -511,9 +575,10 @@ def main():
     ap.add_argument("--chunk-tokens", type=int, default=0,
                     help="split-KV chunk in tokens (multiple of 16); 0 = the planner's choice")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--l2-flush", default="write", choices=["write", "write_read"],
-                    help="between steps: write 512 MB (default), or write 512 MB and then "
-                         "read another 512 MB so no dirty lines are left in L2")
+    ap.add_argument("--l2-flush", default="write_read", choices=["write", "write_read"],
+                    help="between steps: write 512 MB and then read another 512 MB, so no "
+                         "dirty line of the flush is written back inside the timed step "
+                         "(default), or only write 512 MB")
     ap.add_argument("--separate-append", action="store_true",
                     help="quantize_append and decode_run as two launches per step")
     args = ap.parse_args()

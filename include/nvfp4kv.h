@@ -73,6 +73,9 @@ typedef enum nvfp4kv_status {
                                            ran out (a copy or product did not
                                            complete in time); the affected
                                            rows are not valid                */
+#define NVFP4KV_FLAG_BAD_LIVE_LENGTH 0x8u /* a live last_page_len was outside
+                                           [1, 16] or left fewer tokens than
+                                           query rows (clamped)              */
 
 const char* nvfp4kv_status_string(int status);
 const char* nvfp4kv_last_error_detail(void);
@@ -147,7 +150,14 @@ typedef struct nvfp4kv_plan_options {
                                  3 tcgen05 (head dims 128 x 128 only)      */
   int32_t num_sms;            /* >0: override the device's SM count          */
   int32_t ctas_per_sm;        /* >0: override the occupancy query            */
-  int32_t reserved[5];
+  int32_t reserved;
+  /* [dev, may be NULL] live lengths: when set, every run of this plan reads
+   * request b's current last_page_len from device_last_page_len[b] when its
+   * kernel starts, instead of the planned one.  The plan then stays valid
+   * across decode steps for as long as every request keeps its page count
+   * (kv_indptr) and its query count; a step that opens a new page needs a
+   * new plan.  The array must stay allocated while the plan is used. */
+  const int32_t* device_last_page_len;
 } nvfp4kv_plan_options;
 
 typedef struct nvfp4kv_plan_info {
@@ -171,6 +181,7 @@ typedef struct nvfp4kv_plan_info {
   uint64_t off_flags, off_units, off_merge_indptr, off_partial_lse,
       off_partial_o;       /* byte offsets inside the workspace              */
   uint64_t off_counters;   /* merge arrival counters (self-resetting)        */
+  const int32_t* device_last_page_len;  /* the plan option, or NULL          */
 } nvfp4kv_plan_info;
 
 /* Build the plan from HOST copies of the batch description.

@@ -25,6 +25,7 @@ ERR_PLAN_MISMATCH = 6
 FLAG_BAD_PAGE_INDEX = 0x1
 FLAG_BAD_APPEND_TARGET = 0x2
 FLAG_COPY_TIMEOUT = 0x4
+FLAG_BAD_LIVE_LENGTH = 0x8
 
 
 class PagedCacheStruct(C.Structure):
@@ -43,7 +44,7 @@ class PagedCacheStruct(C.Structure):
 class PlanOptions(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "causal", "disable_split", "max_splits", "force_chunk_tokens", "kernel",
-        "num_sms", "ctas_per_sm")] + [("reserved", C.c_int32 * 5)]
+        "num_sms", "ctas_per_sm", "reserved")] + [("device_last_page_len", C.c_void_p)]
 
 
 class PlanInfo(C.Structure):
@@ -56,7 +57,8 @@ class PlanInfo(C.Structure):
         ("num_partials", C.c_int64), ("total_kv_pages", C.c_int64)] + [
         (n, C.c_uint64) for n in (
             "workspace_bytes", "plan_host_bytes", "off_flags", "off_units",
-            "off_merge_indptr", "off_partial_lse", "off_partial_o", "off_counters")]
+            "off_merge_indptr", "off_partial_lse", "off_partial_o", "off_counters")] + [
+        ("device_last_page_len", C.c_void_p)]
 
 
 _vp, _i32, _i64, _u64, _f32 = C.c_void_p, C.c_int32, C.c_int64, C.c_uint64, C.c_float

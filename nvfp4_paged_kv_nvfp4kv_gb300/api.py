@@ -126,10 +126,12 @@ def nvfp4kv_dequantize_paged(cache: PagedCache, page_ids, k_out=None, v_out=None
 
 class Plan:
     """A decode plan: the C plan_info, its pinned host work list and the
-    device workspace it was uploaded into."""
+    device workspace it was uploaded into (and the live length array it
+    reads, kept alive with it)."""
 
-    def __init__(self, info: PlanInfo, host: torch.Tensor, workspace: torch.Tensor):
-        self.info, self.host, self.workspace = info, host, workspace
+    def __init__(self, info: PlanInfo, host: torch.Tensor, workspace: torch.Tensor,
+                 live=None):
+        self.info, self.host, self.workspace, self.live = info, host, workspace, live
 
     def __getattr__(self, name):
         return getattr(self.info, name)
@@ -155,16 +157,21 @@ def nvfp4kv_decode_plan(qo_indptr, kv_indptr, last_page_len, num_qo_heads: int,
                         force_chunk_tokens: int = 0, kernel: int = 0, num_sms: int = 0,
                         ctas_per_sm: int = 0, device: Optional[int] = None,
                         allocate: bool = True, reuse: Optional[Plan] = None,
+                        device_last_page_len: Optional[torch.Tensor] = None,
                         stream=None) -> Plan:
     """Plan from host copies of the indptrs; allocates the pinned host buffer
     and the device workspace (torch) and uploads the work list.  With
     ``reuse`` the plan is written into that plan's buffers when they are big
-    enough (one library call, no allocation)."""
+    enough (one library call, no allocation).  ``device_last_page_len`` (an
+    int32 device tensor [batch]) makes every run read the current last page
+    lengths from it (the plan stays valid while page and query counts do)."""
     L = _lib.load()
     qo, kv, lp = _host_i32(qo_indptr), _host_i32(kv_indptr), _host_i32(last_page_len)
     batch = int(kv.numel()) - 1
     opts = PlanOptions(int(causal), int(disable_split), int(max_splits),
-                       int(force_chunk_tokens), int(kernel), int(num_sms), int(ctas_per_sm))
+                       int(force_chunk_tokens), int(kernel), int(num_sms), int(ctas_per_sm), 0,
+                       None if device_last_page_len is None
+                       else device_last_page_len.data_ptr())
     info = PlanInfo()
     dev = -1 if device is None else int(device)
     args = (qo.data_ptr(), kv.data_ptr(), lp.data_ptr(), batch, num_qo_heads, num_kv_heads,
@@ -174,7 +181,7 @@ def nvfp4kv_decode_plan(qo_indptr, kv_indptr, last_page_len, num_qo_heads: int,
                                    _ptr(reuse.workspace), reuse.workspace.numel(),
                                    _stream(stream), C.byref(info))
         if st == _lib.OK:
-            return Plan(info, reuse.host, reuse.workspace)
+            return Plan(info, reuse.host, reuse.workspace, device_last_page_len)
         if st != _lib.ERR_WORKSPACE_TOO_SMALL:
             check(st, "nvfp4kv_decode_plan")
     st = L.nvfp4kv_decode_plan(*args, None, 0, None, 0, None, C.byref(info))
@@ -186,13 +193,13 @@ def nvfp4kv_decode_plan(qo_indptr, kv_indptr, last_page_len, num_qo_heads: int,
     if not allocate:
         st = L.nvfp4kv_decode_plan(*args, _ptr(host), nhost, None, 0, None, C.byref(info))
         check(st, "nvfp4kv_decode_plan")
-        return Plan(info, host, None)
+        return Plan(info, host, None, device_last_page_len)
     ws = torch.empty(max(int(info.workspace_bytes), 256), dtype=torch.uint8,
                      device="cuda" if device is None else "cuda:%d" % device)
     st = L.nvfp4kv_decode_plan(*args, _ptr(host), nhost, _ptr(ws), ws.numel(),
                                _stream(stream), C.byref(info))
     check(st, "nvfp4kv_decode_plan")
-    return Plan(info, host, ws)
+    return Plan(info, host, ws, device_last_page_len)
 
 
 def _outputs(plan: Plan, out, lse, device):

@@ -532,6 +532,7 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
   info->off_partial_lse = off_plse;
   info->off_partial_o = off_po;
   info->off_counters = off_counters;
+  info->device_last_page_len = opts.device_last_page_len;
 
   if (host_bytes > 0 && (!plan_host || plan_host_bytes < host_bytes))
     return fail(NVFP4KV_ERR_WORKSPACE_TOO_SMALL, "plan_host needs %llu bytes",
@@ -671,6 +672,7 @@ int attend(const nvfp4kv_plan_info* info, const void* q_bf16, int64_t q_stride_t
   p.partial_lse = reinterpret_cast<float*>(ws + info->off_partial_lse);
   p.counters = reinterpret_cast<int*>(ws + info->off_counters);
   p.flags = reinterpret_cast<uint32_t*>(ws + info->off_flags);
+  p.live_last_page_len = info->device_last_page_len;
   if (nt) {
     p.new_k = static_cast<const uint16_t*>(nt->k);
     p.new_v = static_cast<const uint16_t*>(nt->v);

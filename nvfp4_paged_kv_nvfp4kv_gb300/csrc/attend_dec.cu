@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
     mbar_init_fence();
   }
 
-  const WorkUnit u = p.units[blockIdx.x];
+  const WorkUnit u = load_unit(p);
   const int G = p.group;
   const int R = G * u.qo_len;   // <= 8: one row block
   const int npw = u.num_pages > warp ? (u.num_pages - warp + WARPS - 1) / WARPS : 0;

@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(WARPS * 32) attend_simt_kernel(const AttendPar
   float* sP = reinterpret_cast<float*>(smem + T::MAIN_BYTES + T::Q_BYTES);
   int* sRowLim = reinterpret_cast<int*>(smem + T::MAIN_BYTES + T::Q_BYTES + T::P_BYTES);
 
-  const WorkUnit u = p.units[blockIdx.x];
+  const WorkUnit u = load_unit(p);
   const int G = p.group;
   const int R = G * u.qo_len;
   const int row0 = blockIdx.y * RB;

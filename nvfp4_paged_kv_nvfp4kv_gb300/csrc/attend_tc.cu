@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
   float* sRowF = reinterpret_cast<float*>(smem + T::MAIN_BYTES + T::Q_BYTES);
   int* sRowLim = reinterpret_cast<int*>(sRowF + T::RB);
 
-  const WorkUnit u = p.units[blockIdx.x];
+  const WorkUnit u = load_unit(p);
   const int G = p.group;
   const int R = G * u.qo_len;
   const int row0 = blockIdx.y * T::RB;

@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
   int* s_qamax = reinterpret_cast<int*>(s_corr + N);
   float* s_fin = reinterpret_cast<float*>(s_qamax + N);  // [2N + 1]
 
-  const WorkUnit u = p.units[blockIdx.x];
+  const WorkUnit u = load_unit(p);
   const int G = p.group;
   const int R = G * u.qo_len;
   const int row0 = blockIdx.y * N;

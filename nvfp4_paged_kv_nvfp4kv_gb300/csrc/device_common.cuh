@@ -6,6 +6,8 @@
 
 #include <cuda_runtime.h>
 
+#include "internal.h"
+
 namespace nvfp4kv {
 namespace dev {
 
@@ -171,4 +173,23 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
 }
 
 }  // namespace dev
+
+// The CTA's work unit.  With a live last_page_len the unit's kv_len is the
+// request's current length: its planned whole pages plus the current length
+// of the last page (a value outside [1, 16], or a length below the request's
+// query rows, sets flag 0x8 and is clamped).
+__device__ __forceinline__ WorkUnit load_unit(const AttendParams& p) {
+  WorkUnit u = p.units[blockIdx.x];
+  if (p.live_last_page_len != nullptr) {
+    int lpl = __ldg(p.live_last_page_len + u.b);
+    int len = ((u.kv_len - 1) & ~15) + lpl;
+    if (lpl < 1 || lpl > 16 || len < u.qo_len) {
+      if (threadIdx.x == 0) atomicOr(p.flags, 0x8u);
+      lpl = max(1, min(16, lpl));
+      len = max(u.qo_len, ((u.kv_len - 1) & ~15) + lpl);
+    }
+    u.kv_len = len;
+  }
+  return u;
+}
 }  // namespace nvfp4kv

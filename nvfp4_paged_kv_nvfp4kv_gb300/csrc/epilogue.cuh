@@ -145,7 +145,7 @@ __device__ __forceinline__ void finish_unit(const AttendParams& p, const WorkUni
   }
   if (!partial) return;
 
-  merge_if_last<RB, DV, WARPS * 32, 16>(p, u, row0, R, sFin, tid, [] { __syncthreads(); });
+  merge_if_last<RB, DV, WARPS * 32, 20>(p, u, row0, R, sFin, tid, [] { __syncthreads(); });
 }
 
 }  // namespace nvfp4kv

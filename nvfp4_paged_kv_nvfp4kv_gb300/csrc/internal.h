@@ -61,6 +61,9 @@ struct AttendParams {
   float* partial_lse;   // [num_partials]
   int* counters;        // [pairs * row_blocks] arrival counters (split)
   uint32_t* flags;
+  // when set, request b's current last_page_len (device); the planned page
+  // and query counts still hold, kv_len follows it
+  const int32_t* live_last_page_len;
   // fused append (null when not fused): bf16 K/V of the step's new tokens,
   // row-aligned with the query rows (row qo_begin + i is position
   // kv_len - qo_len + i), and the writable cache with its global scales
