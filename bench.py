@@ -36,7 +36,7 @@ from nvfp4_paged_kv_nvfp4kv_gb300 import workloads as W  # noqa: E402
 METRIC = "NVFP4 paged decode: µs/call, KV tokens/s, achieved HBM GB/s vs GB300 peak"
 UNIT = "KV tokens/s"
 FALLBACK_HBM_GBS = 6800.0
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attend_tc_long_context_decode.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attend_dec_long_context_decode.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "nvfp4_paged_kv_nvfp4kv_gb300", "csrc", f)
                   for f in ("attend_dec.cu", "attend_tc.cu", "append_fused.cuh",
                             "device_common.cuh", "epilogue.cuh", "internal.h", "quantize.cuh",
@@ -218,7 +218,8 @@ def run_gpu(args, world, rank, local):
     rows = int(batch.qo_indptr[-1])
     out = torch.empty((rows, c.num_qo_heads, c.head_dim_vo), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((rows, c.num_qo_heads), dtype=torch.float32, device=dev)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = (torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+             if args.l2_flush != "none" else None)
     flush_r = (torch.zeros(512 << 20, dtype=torch.uint8, device=dev)
                if args.l2_flush == "write_read" else None)
     stream = torch.cuda.current_stream(dev)
@@ -250,6 +251,8 @@ def run_gpu(args, world, rank, local):
         #                             host enqueues the step back to back
 
     def l2_flush():
+        if flush is None:
+            return
         flush.fill_(1)              # evict the cache (write > L2) between steps
         if flush_r is not None:     # then read > L2: the flush's dirty lines are
             flush_r.max()           # written back here, not inside the timed step
@@ -282,83 +285,93 @@ def run_gpu(args, world, rank, local):
     kv_tokens = sum(batch.kv_lens)
     value = kv_tokens * world / (ms_step_max * 1e-3)
 
-    # ---- end to end through the public API with host buffers -------------
-    # Serving makes a plan once per change of the batch's page or query
-    # counts: here one plan with live last-page lengths (plan option
-    # device_last_page_len).  Every step copies its inputs (Q, the new tokens'
-    # K/V, the requests' last page lengths) from one pinned host buffer, runs
-    # the fused append + attention, and copies out and lse back.  The step's
-    # three calls are captured once as a CUDA graph and replayed; the eager
-    # figure issues them every step.
-    def packed(tensors, device):
-        offs, n = [], 0
-        for t in tensors:
-            offs.append(n)
-            n += (t.numel() * t.element_size() + 255) // 256 * 256
-        buf = torch.empty(n, dtype=torch.uint8, device=device,
-                          pin_memory=(device == "cpu"))
-        views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
-                 for o, t in zip(offs, tensors)]
-        return buf, views
-    src = [batch.q, batch.new.k[order].contiguous(), batch.new.v[order].contiguous(),
-           batch.last_page_len.to(torch.int32).contiguous()]
-    if args.separate_append:  # the two-launch step also needs request and position
-        src += [batch.new.batch_idx[order].contiguous(), batch.new.positions[order].contiguous()]
-    h_in, h_views = packed(src, "cpu")
-    for hv, t in zip(h_views, src):
-        hv.copy_(t)
-    d_in, d_views = packed(src, dev)
-    d_q, d_k, d_v, d_lpl = d_views[:4]
-    d_b, d_p = (d_views[4], d_views[5]) if args.separate_append else (None, None)
-    h_res, (h_out, h_lse) = packed([out, lse], "cpu")
-    d_res, (e_out, e_lse) = packed([out, lse], dev)
-    d_in.copy_(h_in)
-    plan_e = N.nvfp4kv_decode_plan(batch.qo_indptr, batch.kv_indptr, batch.last_page_len,
-                                   c.num_qo_heads, c.num_kv_heads, c.head_dim_qk,
-                                   c.head_dim_vo, causal=c.causal, kernel=args.kernel,
-                                   force_chunk_tokens=args.chunk_tokens, device=local,
-                                   device_last_page_len=d_lpl)
+    def run_e2e():
+        # ---- end to end through the public API with host buffers -------------
+        # Serving makes a plan once per change of the batch's page or query
+        # counts: here one plan with live last-page lengths (plan option
+        # device_last_page_len).  Every step copies its inputs (Q, the new tokens'
+        # K/V, the requests' last page lengths) from one pinned host buffer, runs
+        # the fused append + attention, and copies out and lse back.  The step's
+        # three calls are captured once as a CUDA graph and replayed; the eager
+        # figure issues them every step.
+        def packed(tensors, device):
+            offs, n = [], 0
+            for t in tensors:
+                offs.append(n)
+                n += (t.numel() * t.element_size() + 255) // 256 * 256
+            buf = torch.empty(n, dtype=torch.uint8, device=device,
+                              pin_memory=(device == "cpu"))
+            views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                     for o, t in zip(offs, tensors)]
+            return buf, views
+        src = [batch.q, batch.new.k[order].contiguous(), batch.new.v[order].contiguous(),
+               batch.last_page_len.to(torch.int32).contiguous()]
+        if args.separate_append:  # the two-launch step also needs request and position
+            src += [batch.new.batch_idx[order].contiguous(), batch.new.positions[order].contiguous()]
+        h_in, h_views = packed(src, "cpu")
+        for hv, t in zip(h_views, src):
+            hv.copy_(t)
+        d_in, d_views = packed(src, dev)
+        d_q, d_k, d_v, d_lpl = d_views[:4]
+        d_b, d_p = (d_views[4], d_views[5]) if args.separate_append else (None, None)
+        h_res, (h_out, h_lse) = packed([out, lse], "cpu")
+        d_res, (e_out, e_lse) = packed([out, lse], dev)
+        d_in.copy_(h_in)
+        plan_e = N.nvfp4kv_decode_plan(batch.qo_indptr, batch.kv_indptr, batch.last_page_len,
+                                       c.num_qo_heads, c.num_kv_heads, c.head_dim_qk,
+                                       c.head_dim_vo, causal=c.causal, kernel=args.kernel,
+                                       force_chunk_tokens=args.chunk_tokens, device=local,
+                                       device_last_page_len=d_lpl)
 
-    def e2e_step():
-        d_in.copy_(h_in, non_blocking=True)
-        if args.separate_append:
-            N.nvfp4kv_quantize_append(cache, d_k, d_v, d_b, d_p, kv_indices, kv_indptr, d_lpl,
-                                      device_flags=flags)
-            N.nvfp4kv_decode_run(plan_e, d_q, cache, kv_indices, batch.sm_scale, out=e_out,
-                                 lse=e_lse)
-        else:
-            N.nvfp4kv_decode_append_run(plan_e, d_k, d_v, d_q, cache, kv_indices,
-                                        batch.sm_scale, out=e_out, lse=e_lse)
-        h_res.copy_(d_res, non_blocking=True)
+        def e2e_step():
+            d_in.copy_(h_in, non_blocking=True)
+            if args.separate_append:
+                N.nvfp4kv_quantize_append(cache, d_k, d_v, d_b, d_p, kv_indices, kv_indptr, d_lpl,
+                                          device_flags=flags)
+                N.nvfp4kv_decode_run(plan_e, d_q, cache, kv_indices, batch.sm_scale, out=e_out,
+                                     lse=e_lse)
+            else:
+                N.nvfp4kv_decode_append_run(plan_e, d_k, d_v, d_q, cache, kv_indices,
+                                            batch.sm_scale, out=e_out, lse=e_lse)
+            h_res.copy_(d_res, non_blocking=True)
 
-    e2e_step()  # eager first call (the library prepares the kernel once)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_steps = max(3, min(args.steps, 200))
-    # bytes moved per step: the packed buffers, with their alignment padding
-    h2d = h_in.numel()
-    d2h = h_res.numel()
+        e2e_step()  # eager first call (the library prepares the kernel once)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_steps = max(3, min(args.steps, 200))
+        # bytes moved per step: the packed buffers, with their alignment padding
+        h2d = h_in.numel()
+        d2h = h_res.numel()
 
-    def time_e2e(run):
-        ts = []
-        for k in range(e2e_steps + 3):
-            l2_flush()
-            torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            run()
-            torch.cuda.synchronize()
-            if k >= 3:
-                ts.append(time.perf_counter() - t0)
-        return ts
-    times = time_e2e(graph.replay)
-    assert torch.equal(h_out.view(torch.int16), out.cpu().view(torch.int16))
-    times_eager = time_e2e(e2e_step)
-    assert torch.equal(h_out.view(torch.int16), out.cpu().view(torch.int16))
-    e2e_s = max_over_ranks(statistics.mean(times), world)
-    e2e_value = kv_tokens * world / e2e_s
+        def time_e2e(run):
+            ts = []
+            for k in range(e2e_steps + 3):
+                l2_flush()
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                run()
+                torch.cuda.synchronize()
+                if k >= 3:
+                    ts.append(time.perf_counter() - t0)
+            return ts
+        times = time_e2e(graph.replay)
+        assert torch.equal(h_out.view(torch.int16), out.cpu().view(torch.int16))
+        times_eager = time_e2e(e2e_step)
+        assert torch.equal(h_out.view(torch.int16), out.cpu().view(torch.int16))
+        e2e_s = max_over_ranks(statistics.mean(times), world)
+        e2e_value = kv_tokens * world / e2e_s
+        return {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
+                "ms_per_step_median": statistics.median(times) * 1e3,
+                "ms_per_step_eager": statistics.mean(times_eager) * 1e3,
+                "how": "plan with live last-page lengths made once; per step: inputs "
+                       "copied from one pinned host buffer, fused append + attention, out "
+                       "and lse copied back; the three calls replayed as a CUDA graph "
+                       "(ms_per_step_eager: issued eagerly)"}
+    e2e = None if args.no_e2e else run_e2e()
 
     # ---- roofline of the attention kernel -------------------------------
     peak, peak_kind = measured_peak()
@@ -376,10 +389,11 @@ def run_gpu(args, world, rank, local):
             "step": ("quantize_append + decode_run (two launches)" if args.separate_append else
                      "decode_append_run: new tokens quantised into their pages, attention and "
                      "split-KV merge in one launch") + "; plan built once",
-            "l2": ("flushed between steps: 512 MB write, then 512 MB read (no dirty "
-                   "lines of the flush are written back inside the timed step)"
-                   if args.l2_flush == "write_read" else
-                   "flushed between steps (512 MB write)"),
+            "l2": {"write_read": "flushed between steps: 512 MB write, then 512 MB read (no "
+                                 "dirty lines of the flush are written back inside the "
+                                 "timed step)",
+                   "write": "flushed between steps (512 MB write)",
+                   "none": "not flushed (profiler capture; not a timing)"}[args.l2_flush],
             "kernel": {1: "tensor-core mma.sync f16/f32acc",
                        2: "CUDA-core f32",
                        3: "tcgen05.mma f16/f32acc, K_hat in tensor memory"}[plan.info.kernel],
@@ -397,14 +411,7 @@ def run_gpu(args, world, rank, local):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": peak_kind},
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
-                "ms_per_step_median": statistics.median(times) * 1e3,
-                "ms_per_step_eager": statistics.mean(times_eager) * 1e3,
-                "how": "plan with live last-page lengths made once; per step: inputs "
-                       "copied from one pinned host buffer, fused append + attention, out "
-                       "and lse copied back; the three calls replayed as a CUDA graph "
-                       "(ms_per_step_eager: issued eagerly)"},
+        "e2e": e2e,
         "gpu_launches": args.steps * (2 if args.separate_append else 1),
         "clocks": clk.summary(),
     }
@@ -575,10 +582,13 @@ def main():
     ap.add_argument("--chunk-tokens", type=int, default=0,
                     help="split-KV chunk in tokens (multiple of 16); 0 = the planner's choice")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--l2-flush", default="write_read", choices=["write", "write_read"],
+    ap.add_argument("--l2-flush", default="write_read", choices=["write", "write_read", "none"],
                     help="between steps: write 512 MB and then read another 512 MB, so no "
                          "dirty line of the flush is written back inside the timed step "
-                         "(default), or only write 512 MB")
+                         "(default), or only write 512 MB; 'none' is for profiler "
+                         "captures, which flush the cache themselves (not a timing mode)")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end leg (profiler captures)")
     ap.add_argument("--separate-append", action="store_true",
                     help="quantize_append and decode_run as two launches per step")
     args = ap.parse_args()
