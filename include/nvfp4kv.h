@@ -91,7 +91,7 @@ typedef struct nvfp4kv_paged_cache {
   int64_t k_sf_stride_page, k_sf_stride_slot, k_sf_stride_head; /* bytes */
   int64_t v_sf_stride_page, v_sf_stride_slot, v_sf_stride_head; /* bytes */
   int32_t num_pages;   /* pages in the pool                                  */
-  int32_t page_size;   /* tokens per page; must be 16                        */
+  int32_t page_size;   /* tokens per page: 16 or 1                           */
   int32_t num_kv_heads;
   int32_t head_dim_qk; /* (Dk, Dv) in {(64,64), (128,128), (256,256),        */
   int32_t head_dim_vo; /*  (256,128), (512,256)}; others: UNSUPPORTED         */
@@ -131,11 +131,13 @@ int nvfp4kv_quantize_append(const nvfp4kv_paged_cache* cache,
                             uint32_t* device_flags, cudaStream_t stream);
 
 /* ---- plan ---------------------------------------------------------------- */
-/* Split-KV (flash-decoding) work plan.  Chunk boundaries are whole pages,
- * i.e. multiples of 16 tokens (page "Re-enable split-KV for NVFP4 KV cache in
- * prefill path": the commit gating split-KV off for NVFP4 and its follow-up
- * asking for 16-token-aligned chunks; a later commit there notes that scale
- * blocks run along head_dim, so a token-axis split never cuts one).  The
+/* Split-KV (flash-decoding) work plan.  Chunk boundaries are multiples of 16
+ * tokens: whole pages at page size 16, sixteen pages at page size 1 (page
+ * "Re-enable split-KV for NVFP4 KV cache in prefill path": the commit gating
+ * split-KV off for NVFP4 and its follow-up asking for 16-token-aligned
+ * chunks; a later commit there notes that scale blocks run along head_dim, so
+ * a token-axis split never cuts one; the tests there run page sizes 1 and
+ * 16).  The
  * plan sizes the chunk so the attention grid fills the GPU in one wave,
  * reading the SM count and the per-block shared-memory opt-in of the device
  * (same page, commit on the shared-memory probe). */
@@ -150,7 +152,7 @@ typedef struct nvfp4kv_plan_options {
                                  3 tcgen05 (head dims 128 x 128 only)      */
   int32_t num_sms;            /* >0: override the device's SM count          */
   int32_t ctas_per_sm;        /* >0: override the occupancy query            */
-  int32_t reserved;
+  int32_t out_dtype;          /* output element: 0 bf16 (default), 1 f16      */
   /* [dev, may be NULL] live lengths: when set, every run of this plan reads
    * request b's current last_page_len from device_last_page_len[b] when its
    * kernel starts, instead of the planned one.  The plan then stays valid
@@ -174,6 +176,7 @@ typedef struct nvfp4kv_plan_info {
   int32_t max_units_per_request;
   int32_t total_qo_rows;   /* sum of n_b                                     */
   int32_t num_sms, ctas_per_sm, smem_bytes, device;
+  int32_t out_dtype;       /* 0 bf16, 1 f16 (the plan option)                */
   int64_t num_partials;    /* partial (o, lse) states when split             */
   int64_t total_kv_pages;  /* pages referenced by the batch                  */
   uint64_t workspace_bytes;  /* device workspace needed                      */
@@ -211,6 +214,8 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
                         nvfp4kv_plan_info* info);
 
 /* ---- run ------------------------------------------------------------------ */
+/* The output element is the plan's out_dtype: bf16 (default) or f16; every
+ * `out_bf16` argument below points to elements of that type. */
 /* Attention for the planned batch: GQA-grouped QK^T, online softmax and PV
  * over the dequantised pages.  When the plan split a request, every work unit
  * stores an f32 partial (o, lse) in the workspace and the last unit of each
@@ -282,9 +287,11 @@ int nvfp4kv_decode_merge(const nvfp4kv_plan_info* info, void* workspace,
  * copy): x_hat = e2m1(code) * E4M3(scale) * global_scale, the exact value
  * rounded to float32 (code * scale is exact; one rounding).
  *   page_ids [dev] int32 [num_ids]: physical page of each entry;
- *   k_out [dev, may be NULL] float32 [num_ids, 16, num_kv_heads, head_dim_qk]:
- *     element (e, slot, h, d) = K of page page_ids[e], slot, head h, dim d;
- *   v_out [dev, may be NULL] float32 [num_ids, 16, num_kv_heads, head_dim_vo];
+ *   k_out [dev, may be NULL] float32 [num_ids, page_size, num_kv_heads,
+ *     head_dim_qk]: element (e, slot, h, d) = K of page page_ids[e], slot,
+ *     head h, dim d;
+ *   v_out [dev, may be NULL] float32 [num_ids, page_size, num_kv_heads,
+ *     head_dim_vo];
  *   device_flags [dev, may be NULL]: NVFP4KV_FLAG_BAD_PAGE_INDEX is or-ed in
  *     for an id outside [0, num_pages); that entry's slots are written as 0.
  * Every slot of a page is converted, including slots past a request's

@@ -44,7 +44,7 @@ class PagedCacheStruct(C.Structure):
 class PlanOptions(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "causal", "disable_split", "max_splits", "force_chunk_tokens", "kernel",
-        "num_sms", "ctas_per_sm", "reserved")] + [("device_last_page_len", C.c_void_p)]
+        "num_sms", "ctas_per_sm", "out_dtype")] + [("device_last_page_len", C.c_void_p)]
 
 
 class PlanInfo(C.Structure):
@@ -53,7 +53,7 @@ class PlanInfo(C.Structure):
         "page_size", "causal", "kernel", "num_units", "row_blocks",
         "rows_per_block", "warps", "split", "chunk_pages",
         "max_units_per_request", "total_qo_rows", "num_sms", "ctas_per_sm",
-        "smem_bytes", "device")] + [
+        "smem_bytes", "device", "out_dtype")] + [
         ("num_partials", C.c_int64), ("total_kv_pages", C.c_int64)] + [
         (n, C.c_uint64) for n in (
             "workspace_bytes", "plan_host_bytes", "off_flags", "off_units",

@@ -105,15 +105,15 @@ def nvfp4kv_quantize_append(cache: PagedCache, k: torch.Tensor, v: torch.Tensor,
 def nvfp4kv_dequantize_paged(cache: PagedCache, page_ids, k_out=None, v_out=None,
                              want_k=True, want_v=True, device_flags=None, stream=None):
     """Dequantise the listed pages to float32: returns (k, v), each
-    [len(page_ids), 16, Hkv, D] (or None when not wanted)."""
+    [len(page_ids), page_size, Hkv, D] (or None when not wanted)."""
     L = _lib.load()
     n = int(page_ids.numel())
     dev = cache.k_data.device
     if want_k and k_out is None:
-        k_out = torch.empty((n, 16, cache.num_kv_heads, cache.head_dim_qk),
+        k_out = torch.empty((n, cache.page_size, cache.num_kv_heads, cache.head_dim_qk),
                             dtype=torch.float32, device=dev)
     if want_v and v_out is None:
-        v_out = torch.empty((n, 16, cache.num_kv_heads, cache.head_dim_vo),
+        v_out = torch.empty((n, cache.page_size, cache.num_kv_heads, cache.head_dim_vo),
                             dtype=torch.float32, device=dev)
     s = cache.struct()
     st = L.nvfp4kv_dequantize_paged(C.byref(s), _ptr(page_ids), n,
@@ -158,18 +158,22 @@ def nvfp4kv_decode_plan(qo_indptr, kv_indptr, last_page_len, num_qo_heads: int,
                         ctas_per_sm: int = 0, device: Optional[int] = None,
                         allocate: bool = True, reuse: Optional[Plan] = None,
                         device_last_page_len: Optional[torch.Tensor] = None,
-                        stream=None) -> Plan:
+                        out_dtype: torch.dtype = torch.bfloat16, stream=None) -> Plan:
     """Plan from host copies of the indptrs; allocates the pinned host buffer
     and the device workspace (torch) and uploads the work list.  With
     ``reuse`` the plan is written into that plan's buffers when they are big
     enough (one library call, no allocation).  ``device_last_page_len`` (an
     int32 device tensor [batch]) makes every run read the current last page
-    lengths from it (the plan stays valid while page and query counts do)."""
+    lengths from it (the plan stays valid while page and query counts do).
+    ``out_dtype`` is torch.bfloat16 (default) or torch.float16."""
+    if out_dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("out_dtype must be torch.bfloat16 or torch.float16")
     L = _lib.load()
     qo, kv, lp = _host_i32(qo_indptr), _host_i32(kv_indptr), _host_i32(last_page_len)
     batch = int(kv.numel()) - 1
     opts = PlanOptions(int(causal), int(disable_split), int(max_splits),
-                       int(force_chunk_tokens), int(kernel), int(num_sms), int(ctas_per_sm), 0,
+                       int(force_chunk_tokens), int(kernel), int(num_sms), int(ctas_per_sm),
+                       1 if out_dtype == torch.float16 else 0,
                        None if device_last_page_len is None
                        else device_last_page_len.data_ptr())
     info = PlanInfo()
@@ -205,7 +209,8 @@ def nvfp4kv_decode_plan(qo_indptr, kv_indptr, last_page_len, num_qo_heads: int,
 def _outputs(plan: Plan, out, lse, device):
     rows, hq, dv = plan.info.total_qo_rows, plan.info.num_qo_heads, plan.info.head_dim_vo
     if out is None:
-        out = torch.empty((rows, hq, dv), dtype=torch.bfloat16, device=device)
+        dt = torch.float16 if plan.info.out_dtype == 1 else torch.bfloat16
+        out = torch.empty((rows, hq, dv), dtype=dt, device=device)
     if lse is None:
         lse = torch.empty((rows, hq), dtype=torch.float32, device=device)
     return out, lse

@@ -77,8 +77,8 @@ int check_cache(const nvfp4kv_paged_cache* c, bool for_attention) {
   if (!c) return fail(NVFP4KV_ERR_INVALID_ARGUMENT, "cache is null");
   if (!c->k_data || !c->v_data || !c->k_sf || !c->v_sf)
     return fail(NVFP4KV_ERR_INVALID_ARGUMENT, "cache buffer pointer is null");
-  if (c->page_size != kPageSize)
-    return fail(NVFP4KV_ERR_UNSUPPORTED, "page_size %d (only 16 is supported)", c->page_size);
+  if (c->page_size != kPageSize && c->page_size != 1)
+    return fail(NVFP4KV_ERR_UNSUPPORTED, "page_size %d (16 and 1 are supported)", c->page_size);
   if (c->num_pages <= 0 || c->num_kv_heads <= 0)
     return fail(NVFP4KV_ERR_INVALID_ARGUMENT, "num_pages %d / num_kv_heads %d must be > 0",
                 c->num_pages, c->num_kv_heads);
@@ -202,6 +202,7 @@ int nvfp4kv_dequantize_paged(const nvfp4kv_paged_cache* cache, const int32_t* pa
   p.num_kv_heads = cache->num_kv_heads;
   p.head_dim_qk = cache->head_dim_qk;
   p.head_dim_vo = cache->head_dim_vo;
+  p.page_size = cache->page_size;
   p.k_global_scale = cache->k_global_scale;
   p.v_global_scale = cache->v_global_scale;
   p.page_ids = page_ids;
@@ -247,6 +248,7 @@ int nvfp4kv_quantize_append(const nvfp4kv_paged_cache* cache, const void* k_bf16
   p.num_kv_heads = cache->num_kv_heads;
   p.head_dim_qk = cache->head_dim_qk;
   p.head_dim_vo = cache->head_dim_vo;
+  p.page_size = cache->page_size;
   p.k_global_scale = cache->k_global_scale;
   p.v_global_scale = cache->v_global_scale;
   p.k = static_cast<const uint16_t*>(k_bf16);
@@ -285,8 +287,10 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
     return fail(NVFP4KV_ERR_INVALID_ARGUMENT,
                 "num_qo_heads %d must be a positive multiple of num_kv_heads %d",
                 num_qo_heads, num_kv_heads);
-  if (page_size != kPageSize)
-    return fail(NVFP4KV_ERR_UNSUPPORTED, "page_size %d (only 16 is supported)", page_size);
+  if (page_size != kPageSize && page_size != 1)
+    return fail(NVFP4KV_ERR_UNSUPPORTED, "page_size %d (16 and 1 are supported)", page_size);
+  if (opts.out_dtype != 0 && opts.out_dtype != 1)
+    return fail(NVFP4KV_ERR_UNSUPPORTED, "out_dtype %d (0 bf16, 1 f16)", opts.out_dtype);
   if (!attention_dims_supported(head_dim_qk, head_dim_vo))
     return fail(NVFP4KV_ERR_UNSUPPORTED, "attention head dims (%d, %d) not built",
                 head_dim_qk, head_dim_vo);
@@ -302,7 +306,10 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
   // ---- batch description ------------------------------------------------
   if (batch > 0 && qo_indptr_h[0] != 0)
     return fail(NVFP4KV_ERR_INVALID_ARGUMENT, "qo_indptr[0] must be 0");
-  std::vector<int32_t> np(batch), nq(batch);
+  // the planner counts 16-token tiles: one page at page size 16, PT pages
+  // at page size 1
+  const int PT = kPageSize / page_size;
+  std::vector<int32_t> np(batch), nq(batch), nt(batch);
   int64_t total_pages = 0;
   int max_rows = 0, max_np = 0;
   for (int b = 0; b < batch; ++b) {
@@ -314,11 +321,12 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
       return fail(NVFP4KV_ERR_INVALID_ARGUMENT, "kv_indptr[%d] < 0", b);
     int64_t L = 0;
     if (np[b] > 0) {
-      if (last_page_len_h[b] < 1 || last_page_len_h[b] > kPageSize)
-        return fail(NVFP4KV_ERR_INVALID_ARGUMENT, "last_page_len[%d] = %d not in [1, 16]", b,
-                    last_page_len_h[b]);
-      L = static_cast<int64_t>(np[b] - 1) * kPageSize + last_page_len_h[b];
+      if (last_page_len_h[b] < 1 || last_page_len_h[b] > page_size)
+        return fail(NVFP4KV_ERR_INVALID_ARGUMENT, "last_page_len[%d] = %d not in [1, %d]", b,
+                    last_page_len_h[b], page_size);
+      L = static_cast<int64_t>(np[b] - 1) * page_size + last_page_len_h[b];
     }
+    nt[b] = (np[b] + PT - 1) / PT;
     if (L < nq[b])
       return fail(NVFP4KV_ERR_INVALID_ARGUMENT,
                   "request %d has %d query rows but only %lld kv tokens", b, nq[b],
@@ -327,7 +335,7 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
       return fail(NVFP4KV_ERR_UNSUPPORTED, "request %d longer than 2^30 tokens", b);
     if (nq[b] > 0) {
       total_pages += np[b];
-      max_np = std::max(max_np, np[b]);
+      max_np = std::max(max_np, nt[b]);  // in tiles from here on
       max_rows = std::max(max_rows, nq[b] * G);
     }
   }
@@ -399,12 +407,12 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
     info->device = device;
   }
 
-  // ---- chunk size (pages per unit) --------------------------------------
+  // ---- chunk size (tiles per unit) --------------------------------------
   auto row_blocks_of = [&](int b) { return (nq[b] * G + rows_per_block - 1) / rows_per_block; };
   auto ctas_for = [&](int64_t c) {
     int64_t n = 0;
     for (int b = 0; b < batch; ++b)
-      if (nq[b] > 0) n += (int64_t)num_kv_heads * ((np[b] + c - 1) / c) * row_blocks_of(b);
+      if (nq[b] > 0) n += (int64_t)num_kv_heads * ((nt[b] + c - 1) / c) * row_blocks_of(b);
     return n;
   };
   int64_t chunk = std::max(max_np, 1);
@@ -415,7 +423,7 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
       const int64_t slots = (int64_t)num_sms * ctas_per_sm;
       int64_t work = 0;
       for (int b = 0; b < batch; ++b)
-        if (nq[b] > 0) work += (int64_t)num_kv_heads * np[b] * row_blocks_of(b);
+        if (nq[b] > 0) work += (int64_t)num_kv_heads * nt[b] * row_blocks_of(b);
       int64_t lo = std::max<int64_t>(kMinChunkPages, (work + slots - 1) / std::max<int64_t>(slots, 1));
       int64_t hi = max_np;
       if (lo >= hi || ctas_for(hi) > slots) {
@@ -443,8 +451,8 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
   int64_t n_units = 0;
   for (int b = 0; b < batch; ++b)
     if (nq[b] > 0) {
-      if (np[b] > chunk) split = true;
-      n_units += (int64_t)num_kv_heads * ((np[b] + chunk - 1) / chunk);
+      if (nt[b] > chunk) split = true;
+      n_units += (int64_t)num_kv_heads * ((nt[b] + chunk - 1) / chunk);
     }
   units.reserve(static_cast<size_t>(n_units));
   int64_t partial = 0;
@@ -452,19 +460,20 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
   std::vector<int32_t> nsplit(batch, 0);
   for (int b = 0; b < batch; ++b) {
     if (nq[b] == 0) continue;
-    const int S = static_cast<int>((np[b] + chunk - 1) / chunk);
+    const int S = static_cast<int>((nt[b] + chunk - 1) / chunk);
     nsplit[b] = S;
     max_units = std::max(max_units, S);
     pbase[b] = partial;
     if (split) partial += (int64_t)nq[b] * num_qo_heads * S;
-    const int64_t L = static_cast<int64_t>(np[b] - 1) * kPageSize + last_page_len_h[b];
+    const int64_t L = static_cast<int64_t>(np[b] - 1) * page_size + last_page_len_h[b];
+    const int64_t cp = chunk * PT;  // pages per unit
     for (int h = 0; h < num_kv_heads; ++h)
       for (int s = 0; s < S; ++s) {
         WorkUnit u{};
         u.b = b;
         u.h_kv = h;
-        u.page_begin = kv_indptr_h[b] + static_cast<int32_t>(s * chunk);
-        u.num_pages = static_cast<int32_t>(std::min<int64_t>(chunk, np[b] - s * chunk));
+        u.page_begin = kv_indptr_h[b] + static_cast<int32_t>(s * cp);
+        u.num_pages = static_cast<int32_t>(std::min<int64_t>(cp, np[b] - s * cp));
         u.tok_begin = static_cast<int32_t>(s * chunk * kPageSize);
         u.kv_len = static_cast<int32_t>(L);
         u.qo_begin = qo_indptr_h[b];
@@ -521,6 +530,7 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
   info->total_qo_rows = total_rows;
   info->num_sms = num_sms;
   info->ctas_per_sm = ctas_per_sm;
+  info->out_dtype = opts.out_dtype;
   info->smem_bytes = cfg.smem_bytes;
   info->num_partials = partial;
   info->total_kv_pages = total_pages;
@@ -643,7 +653,7 @@ int attend(const nvfp4kv_plan_info* info, const void* q_bf16, int64_t q_stride_t
   // kernel when the cache layout allows it (same arithmetic, same occupancy
   // or better: the plan's one-wave grid stays one wave)
   const bool dec = info->kernel == kKernelTensorCore && info->rows_per_block == 8 &&
-                   bulk_decode_layout(cache) &&
+                   info->page_size == kPageSize && bulk_decode_layout(cache) &&
                    attend_config_dec(info->head_dim_qk, info->head_dim_vo, 8, &cfg);
   if (!dec && !lookup_kernel(info->kernel, info->head_dim_qk, info->head_dim_vo,
                              info->rows_per_block, &cfg))
@@ -663,6 +673,8 @@ int attend(const nvfp4kv_plan_info* info, const void* q_bf16, int64_t q_stride_t
   p.group = info->num_qo_heads / info->num_kv_heads;
   p.causal = info->causal;
   p.split = info->split;
+  p.page_size = info->page_size;
+  p.out_f16 = info->out_dtype == 1;
   p.qk_scale_log2 = static_cast<float>(static_cast<double>(sm_scale) *
                                        cache->k_global_scale * 1.4426950408889634);
   p.v_scale = cache->v_global_scale;
@@ -736,7 +748,7 @@ int nvfp4kv_decode_merge(const nvfp4kv_plan_info* info, void* workspace,
       reinterpret_cast<const float*>(ws + info->off_partial_lse),
       reinterpret_cast<const int32_t*>(ws + info->off_merge_indptr),
       static_cast<int32_t>((int64_t)info->total_qo_rows * info->num_qo_heads),
-      info->head_dim_vo, static_cast<uint16_t*>(out_bf16), lse, stream);
+      info->head_dim_vo, static_cast<uint16_t*>(out_bf16), lse, info->out_dtype == 1, stream);
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   return ok();
 }
@@ -765,7 +777,7 @@ int nvfp4kv_merge_states(const float* o_partial, const float* lse_partial,
   if (!aligned(o_partial, 16) || !aligned(out_bf16, 2))
     return fail(NVFP4KV_ERR_INVALID_ARGUMENT, "o_partial must be 16-byte aligned");
   cudaError_t e = launch_merge(o_partial, lse_partial, merge_indptr, num_entries, head_dim_vo,
-                               static_cast<uint16_t*>(out_bf16), lse, stream);
+                               static_cast<uint16_t*>(out_bf16), lse, false, stream);
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   return ok();
 }

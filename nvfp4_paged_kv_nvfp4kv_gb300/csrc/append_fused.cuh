@@ -34,12 +34,12 @@ __device__ __forceinline__ void append_unit_tokens(const AttendParams& p, const 
                   (int64_t)u.h_kv * p.nk_stride_head;
     const uint4 lo16 = *reinterpret_cast<const uint4*>(src + 16 * jb);
     const uint4 hi16 = *reinterpret_cast<const uint4*>(src + 16 * jb + 8);
-    const int32_t page = p.kv_indices[u.page_begin + (tok - u.tok_begin) / 16];
+    const int32_t page = p.kv_indices[u.page_begin + (tok - u.tok_begin) / p.page_size];
     if (page < 0 || page >= p.cache.num_pages) {
       atomicOr(p.flags, 0x2u);
       continue;
     }
-    const int slot = tok % 16;
+    const int slot = tok % p.page_size;
     uint2 packed;
     const uint32_t sfb =
         quantize_block16(lo16, hi16, isv ? p.v_global_scale : p.k_global_scale, &packed);

@@ -95,15 +95,29 @@ __global__ void __launch_bounds__(WARPS * 32) attend_simt_kernel(const AttendPar
 
   uint8_t* wpipe = pipe + warp * STAGES * S::STAGE_BYTES;
   float* wP = sP + warp * RB * 16;
-  const int npw = u.num_pages > warp ? (u.num_pages - warp + WARPS - 1) / WARPS : 0;
+  // tiles of 16 tokens: one page each at page size 16, sixteen 1-token pages
+  // at page size 1 (lane r then copies through the id of row r)
+  const bool rows = p.page_size == 1;
+  const int ntiles = rows ? (u.num_pages + 15) / 16 : u.num_pages;
+  const int npw = ntiles > warp ? (ntiles - warp + WARPS - 1) / WARPS : 0;
   const int32_t* pidx = p.kv_indices + u.page_begin;
   auto load_page = [&](int i) {
-    int32_t pid = pidx[warp + i * WARPS];
+    int32_t pid;
+    if (rows) {
+      const int pg = 16 * (warp + i * WARPS) + (lane & 15);
+      pid = pg < u.num_pages ? pidx[pg] : 0;
+    } else {
+      pid = pidx[warp + i * WARPS];
+    }
     if (pid < 0 || pid >= p.cache.num_pages) {
-      if (lane == 0) atomicOr(p.flags, 0x1u);
+      atomicOr(p.flags, 0x1u);
       pid = 0;
     }
-    issue_page<S>(wpipe + (i % STAGES) * S::STAGE_BYTES, p.cache, pid, u.h_kv, lane);
+    uint8_t* st = wpipe + (i % STAGES) * S::STAGE_BYTES;
+    if (rows)
+      issue_tile_rows<S>(st, p.cache, pid, u.h_kv, lane);
+    else
+      issue_page<S>(st, p.cache, pid, u.h_kv, lane);
   };
 #pragma unroll
   for (int s = 0; s < STAGES - 1; ++s) {

@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
   int new_lo = 0, new_hi = 0;
   if (p.new_k != nullptr) {
     new_lo = max(u.kv_len - u.qo_len, u.tok_begin);
-    new_hi = min(u.kv_len, u.tok_begin + 16 * u.num_pages);
+    new_hi = min(u.kv_len, u.tok_begin + p.page_size * u.num_pages);
   }
   auto append_new = [&]() {
     append_unit_tokens<DK, DV>(p, u, new_lo, new_hi, tid, WARPS * 32);
@@ -157,21 +157,32 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
   // ---- start the page pipeline: the first pages' copies are in flight
   // while Q is prepared ---------------------------------------------------
   uint8_t* wpipe = pipe + warp * STAGES * T::STAGE_BYTES;
-  const int npw = u.num_pages > warp ? (u.num_pages - warp + WARPS - 1) / WARPS : 0;
+  // tiles of 16 tokens: one page each at page size 16, sixteen 1-token pages
+  // at page size 1
+  const bool rows = p.page_size == 1;
+  const int ntiles = rows ? (u.num_pages + 15) / 16 : u.num_pages;
+  const int npw = ntiles > warp ? (ntiles - warp + WARPS - 1) / WARPS : 0;
   const int32_t* pidx = p.kv_indices + u.page_begin;
 
   // page ids are read one iteration before their copies are issued, so the
-  // address computation never waits on a global load
+  // address computation never waits on a global load (page size 1: lane r
+  // reads the id of row r; a row past the unit's pages reads page 0)
   auto page_id = [&](int i) -> int32_t {
-    return i < npw ? pidx[warp + i * WARPS] : 0;
+    if (i >= npw) return 0;
+    if (!rows) return pidx[warp + i * WARPS];
+    const int pg = 16 * (warp + i * WARPS) + (lane & 15);
+    return pg < u.num_pages ? pidx[pg] : 0;
   };
   auto load_page = [&](int i, int32_t pid) {
     if (pid < 0 || pid >= p.cache.num_pages) {
-      if (lane == 0) atomicOr(p.flags, 0x1u);
+      atomicOr(p.flags, 0x1u);
       pid = 0;
     }
-    issue_page<typename T::S>(wpipe + (i % STAGES) * T::STAGE_BYTES, p.cache, pid, u.h_kv,
-                              lane);
+    uint8_t* st = wpipe + (i % STAGES) * T::STAGE_BYTES;
+    if (rows)
+      issue_tile_rows<typename T::S>(st, p.cache, pid, u.h_kv, lane);
+    else
+      issue_page<typename T::S>(st, p.cache, pid, u.h_kv, lane);
   };
 
 #pragma unroll

@@ -54,7 +54,6 @@ namespace {
 using namespace dev;
 
 constexpr int kTileTok = 128;
-constexpr int kTilePages = kTileTok / kPageSize;
 constexpr int kThreads = 544;  // softmax warps 0-7, dequant warps 8-15, issue warp 16
 constexpr int kKB = 3;         // K_hat / V_hat buffers
 constexpr float kRaise = 8.f;  // log2 of the largest p before m is raised
@@ -345,8 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
   const int q4 = warp & 3;                        // tensor-memory lane quarter
   const int j = 32 * q4 + lane;                   // token of the tile / value dim
   const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-  const int ntiles = (u.num_pages + kTilePages - 1) / kTilePages;
-  const int tok_end = min(u.kv_len, u.tok_begin + kPageSize * u.num_pages);
+  const int unit_tok = p.page_size * u.num_pages;  // tokens the unit's pages hold
+  const int ntiles = (unit_tok + kTileTok - 1) / kTileTok;
+  const int tok_end = min(u.kv_len, u.tok_begin + unit_tok);
 
   if (tid == 0) {
     for (int b = 0; b < kKB; ++b) {
@@ -384,12 +384,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
     // ================= dequant (thread = token, half the dims) ===========
     const CacheView& c = p.cache;
     const int hd = (warp - 8) >> 2;  // dims [64 hd, 64 hd + 64)
-    const int slot = j & 15;
+    // this thread's token j of tile t: page rel / page_size, slot rel % page_size
     uint8_t* wst = sRaw + (warp - 8) * T::WST;
     // stage layout per warp: K chunks [2][32][16], V chunks [2][32][16],
     // K scales [32][4], V scales [32][4]
     auto issue = [&](int t) {
-      const int pg = t * kTilePages + (j >> 4);
+      const int rel = t * kTileTok + j;
+      const int pg = rel / p.page_size, slot = rel % p.page_size;
       if (pg >= u.num_pages) return;
       int32_t pid = p.kv_indices[u.page_begin + pg];
       if (pid < 0 || pid >= c.num_pages) {
@@ -794,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
               const int qi = gr / G, head = u.h_kv * G + gr % G;
               const int64_t qrow = u.qo_begin + qi;
               if (!partial) {
-                p.out[(qrow * Hq + head) * DV + j] = f32_to_bf16_bits(o);
+                p.out[(qrow * Hq + head) * DV + j] = pack_out1(o, p.out_f16);
                 if (j == 0 && p.lse) p.lse[qrow * Hq + head] = lse_v;
               } else {
                 const int64_t pi = (int64_t)u.partial_base +

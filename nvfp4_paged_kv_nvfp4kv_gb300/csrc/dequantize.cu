@@ -27,15 +27,15 @@ __global__ void __launch_bounds__(256) dequantize_kernel(const DequantParams p) 
   const int bpk = p.k_out ? p.head_dim_qk / 16 : 0;
   const int bpv = p.v_out ? p.head_dim_vo / 16 : 0;
   const int per = bpk + bpv;
-  const int64_t total = static_cast<int64_t>(p.num_ids) * kPageSize * p.num_kv_heads * per;
+  const int64_t total = static_cast<int64_t>(p.num_ids) * p.page_size * p.num_kv_heads * per;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int blk = static_cast<int>(idx % per);
     const int64_t rest = idx / per;
     const int h = static_cast<int>(rest % p.num_kv_heads);
-    const int64_t ps = rest / p.num_kv_heads;  // page entry * 16 + slot
-    const int slot = static_cast<int>(ps % kPageSize);
-    const int64_t e = ps / kPageSize;
+    const int64_t ps = rest / p.num_kv_heads;  // page entry * page_size + slot
+    const int slot = static_cast<int>(ps % p.page_size);
+    const int64_t e = ps / p.page_size;
     const bool isv = blk >= bpk;
     const int jb = isv ? blk - bpk : blk;
     const int d = isv ? p.head_dim_vo : p.head_dim_qk;
@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(256) dequantize_kernel(const DequantParams p) 
 
 cudaError_t launch_dequantize(const DequantParams& p, cudaStream_t stream) {
   const int per = (p.k_out ? p.head_dim_qk / 16 : 0) + (p.v_out ? p.head_dim_vo / 16 : 0);
-  const int64_t total = static_cast<int64_t>(p.num_ids) * kPageSize * p.num_kv_heads * per;
+  const int64_t total = static_cast<int64_t>(p.num_ids) * p.page_size * p.num_kv_heads * per;
   if (total == 0) return cudaSuccess;
   const int threads = 256;
   int64_t blocks = (total + threads - 1) / threads;

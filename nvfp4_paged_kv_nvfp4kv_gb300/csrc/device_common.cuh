@@ -176,20 +176,31 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
 
 // The CTA's work unit.  With a live last_page_len the unit's kv_len is the
 // request's current length: its planned whole pages plus the current length
-// of the last page (a value outside [1, 16], or a length below the request's
-// query rows, sets flag 0x8 and is clamped).
+// of the last page (a value outside [1, page_size], or a length below the
+// request's query rows, sets flag 0x8 and is clamped).
 __device__ __forceinline__ WorkUnit load_unit(const AttendParams& p) {
   WorkUnit u = p.units[blockIdx.x];
   if (p.live_last_page_len != nullptr) {
+    const int P = p.page_size;
+    const int full = (u.kv_len - 1) - (u.kv_len - 1) % P;  // tokens in whole pages
     int lpl = __ldg(p.live_last_page_len + u.b);
-    int len = ((u.kv_len - 1) & ~15) + lpl;
-    if (lpl < 1 || lpl > 16 || len < u.qo_len) {
+    int len = full + lpl;
+    if (lpl < 1 || lpl > P || len < u.qo_len) {
       if (threadIdx.x == 0) atomicOr(p.flags, 0x8u);
-      lpl = max(1, min(16, lpl));
-      len = max(u.qo_len, ((u.kv_len - 1) & ~15) + lpl);
+      lpl = max(1, min(P, lpl));
+      len = max(u.qo_len, full + lpl);
     }
     u.kv_len = len;
   }
   return u;
+}
+
+// Two f32 values as two packed output elements (bf16 or f16, lo from a).
+__device__ __forceinline__ uint32_t pack_out2(float a, float b, bool f16) {
+  return f16 ? dev::f32x2_to_f16x2(a, b)
+             : ((uint32_t)dev::f32_to_bf16_bits(a) | ((uint32_t)dev::f32_to_bf16_bits(b) << 16));
+}
+__device__ __forceinline__ uint16_t pack_out1(float a, bool f16) {
+  return f16 ? (uint16_t)(dev::f32x2_to_f16x2(a, 0.f) & 0xFFFFu) : dev::f32_to_bf16_bits(a);
 }
 }  // namespace nvfp4kv

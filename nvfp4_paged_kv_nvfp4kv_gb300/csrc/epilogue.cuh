@@ -84,10 +84,8 @@ __device__ __forceinline__ void merge_if_last(const AttendParams& p, const WorkU
     const float inv = any ? 1.f / L : 0.f;
     const int64_t qrow = u.qo_begin + i;
     uint32_t* dst = reinterpret_cast<uint32_t*>(p.out + (qrow * Hq + head) * DV + 4 * d4);
-    dst[0] = (uint32_t)f32_to_bf16_bits(acc.x * inv) |
-             ((uint32_t)f32_to_bf16_bits(acc.y * inv) << 16);
-    dst[1] = (uint32_t)f32_to_bf16_bits(acc.z * inv) |
-             ((uint32_t)f32_to_bf16_bits(acc.w * inv) << 16);
+    dst[0] = pack_out2(acc.x * inv, acc.y * inv, p.out_f16);
+    dst[1] = pack_out2(acc.z * inv, acc.w * inv, p.out_f16);
     if (d4 == 0 && p.lse) p.lse[qrow * Hq + head] = any ? (M + log2f(L)) * kLn2 : -INFINITY;
   }
 }
@@ -132,9 +130,8 @@ __device__ __forceinline__ void finish_unit(const AttendParams& p, const WorkUni
     const int i = r / G, head = u.h_kv * G + r % G;
     const int64_t qrow = u.qo_begin + i;
     if (!partial) {
-      const uint32_t packed =
-          (uint32_t)f32_to_bf16_bits(o0) | ((uint32_t)f32_to_bf16_bits(o1) << 16);
-      *reinterpret_cast<uint32_t*>(p.out + (qrow * Hq + head) * DV + d) = packed;
+      *reinterpret_cast<uint32_t*>(p.out + (qrow * Hq + head) * DV + d) =
+          pack_out2(o0, o1, p.out_f16);
       if (d == 0 && p.lse) p.lse[qrow * Hq + head] = lse_v;
     } else {
       const int64_t pi = (int64_t)u.partial_base +

@@ -9,12 +9,14 @@
 namespace nvfp4kv {
 
 constexpr uint32_t kPlanMagic = 0x4E564B50u;  // "NVKP"
-constexpr int kPageSize = 16;
+constexpr int kPageSize = 16;  // tokens of one tile (one page at page size 16)
 constexpr int kBlock = 16;  // elements per E4M3 scale
 
 // One attention work unit: the pages [page_begin, page_begin + num_pages)
 // of kv_indices belong to request b; the unit covers its tokens
-// [tok_begin, tok_begin + 16*num_pages) clipped to kv_len.  The partial state
+// [tok_begin, tok_begin + page_size*num_pages) clipped to kv_len, walked in
+// tiles of 16 tokens (one page at page size 16, sixteen at page size 1;
+// tok_begin is a multiple of 16).  The partial state
 // of query row i, head h (of the unit's kv head) lives at
 //   partial_base + (i * Hq + h) * num_splits + split      (when split),
 // and `pair` numbers the (request, kv head) for the merge counters.
@@ -53,9 +55,11 @@ struct AttendParams {
   const int32_t* kv_indices;
   const WorkUnit* units;
   int32_t num_qo_heads, group, causal, split;
+  int32_t page_size;    // 16 or 1
+  int32_t out_f16;      // output element: 0 bf16, 1 f16
   float qk_scale_log2;  // sm_scale * k_global_scale * log2(e)
   float v_scale;        // v_global_scale
-  uint16_t* out;        // bf16 [rows, Hq, Dv]
+  uint16_t* out;        // bf16 or f16 [rows, Hq, Dv]
   float* lse;           // [rows, Hq] or null
   float* partial_o;     // [num_partials, Dv]
   float* partial_lse;   // [num_partials]
@@ -80,7 +84,7 @@ struct AppendParams {
   uint8_t* v_sf;
   int64_t k_sp, k_ss, k_sh, v_sp, v_ss, v_sh;
   int64_t ksf_sp, ksf_ss, ksf_sh, vsf_sp, vsf_ss, vsf_sh;
-  int32_t num_pages, num_kv_heads, head_dim_qk, head_dim_vo;
+  int32_t num_pages, num_kv_heads, head_dim_qk, head_dim_vo, page_size;
   float k_global_scale, v_global_scale;
   const uint16_t* k;
   const uint16_t* v;
@@ -101,12 +105,12 @@ struct DequantParams {
   const uint8_t* v_sf;
   int64_t k_sp, k_ss, k_sh, v_sp, v_ss, v_sh;
   int64_t ksf_sp, ksf_ss, ksf_sh, vsf_sp, vsf_ss, vsf_sh;
-  int32_t num_pages, num_kv_heads, head_dim_qk, head_dim_vo;
+  int32_t num_pages, num_kv_heads, head_dim_qk, head_dim_vo, page_size;
   float k_global_scale, v_global_scale;
   const int32_t* page_ids;
   int32_t num_ids;
-  float* k_out;  // [num_ids, 16, Hkv, Dk] or null
-  float* v_out;  // [num_ids, 16, Hkv, Dv] or null
+  float* k_out;  // [num_ids, page_size, Hkv, Dk] or null
+  float* v_out;  // [num_ids, page_size, Hkv, Dv] or null
   uint32_t* flags;
 };
 
@@ -130,7 +134,7 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_dequantize(const DequantParams& p, cudaStream_t stream);
 cudaError_t launch_merge(const float* o_partial, const float* lse_partial,
                          const int32_t* merge_indptr, int32_t num_entries,
-                         int32_t head_dim_vo, uint16_t* out, float* lse,
+                         int32_t head_dim_vo, uint16_t* out, float* lse, bool out_f16,
                          cudaStream_t stream);
 
 }  // namespace nvfp4kv

@@ -20,7 +20,7 @@ template <int PER>
 __global__ void __launch_bounds__(256)
     merge_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                  const int32_t* __restrict__ indptr, int32_t n, int32_t dv,
-                 uint16_t* __restrict__ out, float* __restrict__ lse) {
+                 uint16_t* __restrict__ out, float* __restrict__ lse, bool out_f16) {
   const int lane = threadIdx.x & 31;
   const int64_t e = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (e >= n) return;
@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(256)
   }
   uint16_t* dst = out + e * dv + lane * PER;
 #pragma unroll
-  for (int k = 0; k < PER; ++k) dst[k] = dev::f32_to_bf16_bits(acc[k]);
+  for (int k = 0; k < PER; ++k) dst[k] = pack_out1(acc[k], out_f16);
   if (lane == 0 && lse) lse[e] = L;
 }
 
@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(256)
 
 cudaError_t launch_merge(const float* o_partial, const float* lse_partial,
                          const int32_t* merge_indptr, int32_t num_entries,
-                         int32_t head_dim_vo, uint16_t* out, float* lse,
+                         int32_t head_dim_vo, uint16_t* out, float* lse, bool out_f16,
                          cudaStream_t stream) {
   if (num_entries == 0) return cudaSuccess;
   const int warps = 8;
@@ -77,7 +77,7 @@ cudaError_t launch_merge(const float* o_partial, const float* lse_partial,
 #define NVFP4KV_MERGE(PER_)                                                          \
   case PER_:                                                                       \
     merge_kernel<PER_><<<blocks, warps * 32, 0, stream>>>(                         \
-        o_partial, lse_partial, merge_indptr, num_entries, head_dim_vo, out, lse); \
+        o_partial, lse_partial, merge_indptr, num_entries, head_dim_vo, out, lse, out_f16); \
     break;
   switch (per) {
     NVFP4KV_MERGE(1)

@@ -61,10 +61,10 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
     if (ok) {
       const int beg = p.kv_indptr[b];
       const int np = p.kv_indptr[b + 1] - beg;
-      const int64_t L = np > 0 ? static_cast<int64_t>(np - 1) * kPageSize + p.last_page_len[b] : 0;
+      const int64_t L = np > 0 ? static_cast<int64_t>(np - 1) * p.page_size + p.last_page_len[b] : 0;
       ok = pos < L;
       if (ok) {
-        page = p.kv_indices[beg + pos / kPageSize];
+        page = p.kv_indices[beg + pos / p.page_size];
         ok = page >= 0 && page < p.num_pages;
       }
     }
@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
       if (p.flags && blk == 0 && h == 0) atomicOr(p.flags, 0x2u);
       continue;
     }
-    const int slot = pos % kPageSize;
+    const int slot = pos % p.page_size;
 
     const float g = isv ? p.v_global_scale : p.k_global_scale;
     uint2 packed;

@@ -79,4 +79,56 @@ __device__ __forceinline__ void issue_page(uint8_t* st, const CacheView& c, int3
   }
 }
 
+// Page size 1: the 16 token rows of a tile come from 16 pages (slot 0 each).
+// pid_lane: lane r (r < 16) holds the page id of row r (lanes 16-31 repeat
+// lanes 0-15); every lane takes the id of the row it copies by a shuffle,
+// executed by all lanes before the copy's own condition.
+template <class S>
+__device__ __forceinline__ void issue_tile_rows(uint8_t* st, const CacheView& c,
+                                                int32_t pid_lane, int h, int lane) {
+  using namespace dev;
+  constexpr int KCH = S::KROW / 16;
+  constexpr int VCHR = (S::VC * 8) / 16;
+#pragma unroll
+  for (int k = 0; k < (16 * KCH + 31) / 32; ++k) {
+    const int ci = lane + 32 * k;
+    const int r = ci / KCH, ch = ci % KCH;
+    const int32_t pr = __shfl_sync(0xffffffffu, pid_lane, r & 15);
+    if (ci < 16 * KCH)
+      cp_async_16(st + r * S::KROW + S::k_pos(r, ch) * 16,
+                  c.k_data + pr * c.k_sp + h * c.k_sh + ch * 16);
+  }
+#pragma unroll
+  for (int k = 0; k < (16 * VCHR + 31) / 32; ++k) {
+    const int ci = lane + 32 * k;
+    const int r = ci / VCHR, ch = ci % VCHR;
+    const int32_t pr = __shfl_sync(0xffffffffu, pid_lane, r & 15);
+    if (ci < 16 * VCHR)
+      cp_async_16(st + S::OFF_V + r * S::VROW + ch * 16,
+                  c.v_data + pr * c.v_sp + h * c.v_sh + ch * 16);
+  }
+  constexpr int KSU = S::KSFROW < 16 ? S::KSFROW : 16;
+  constexpr int KSN = S::KSFROW / KSU;
+#pragma unroll
+  for (int k = 0; k < (16 * KSN + 31) / 32; ++k) {
+    const int ci = lane + 32 * k;
+    const int r = ci / KSN, u = ci % KSN;
+    const int32_t pr = __shfl_sync(0xffffffffu, pid_lane, r & 15);
+    if (ci < 16 * KSN)
+      cp_async_small<KSU>(st + S::OFF_KSF + r * S::KSFROW + u * KSU,
+                          c.k_sf + pr * c.ksf_sp + h * c.ksf_sh + u * KSU);
+  }
+  constexpr int VSU = S::VSFROW < 16 ? S::VSFROW : 16;
+  constexpr int VSN = S::VSFROW / VSU;
+#pragma unroll
+  for (int k = 0; k < (16 * VSN + 31) / 32; ++k) {
+    const int ci = lane + 32 * k;
+    const int r = ci / VSN, u = ci % VSN;
+    const int32_t pr = __shfl_sync(0xffffffffu, pid_lane, r & 15);
+    if (ci < 16 * VSN)
+      cp_async_small<VSU>(st + S::OFF_VSF + r * S::VSFROW + u * VSU,
+                          c.v_sf + pr * c.vsf_sp + h * c.vsf_sh + u * VSU);
+  }
+}
+
 }  // namespace nvfp4kv

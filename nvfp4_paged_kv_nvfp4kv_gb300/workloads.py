@@ -145,10 +145,11 @@ class Batch:
     k_global_scale: float
     v_global_scale: float
     sm_scale: float
+    page_size: int = PAGE_SIZE
 
     def cache_layout(self, layout="HND", pad_page_bytes=0):
         c = self.cfg
-        return CacheLayout(layout, self.num_pages, PAGE_SIZE,
+        return CacheLayout(layout, self.num_pages, self.page_size,
                            c.num_kv_heads, c.head_dim_qk, c.head_dim_vo,
                            pad_page_bytes)
 
@@ -229,3 +230,26 @@ def make_batch(cfg: Workload, extra_pages: int = 0) -> Batch:
         q=q, prefix=sel(~is_new), new=sel(is_new),
         k_global_scale=gk, v_global_scale=gv,
         sm_scale=1.0 / math.sqrt(Dk))
+
+
+def with_page_size_one(batch: Batch, seed: int = 7, extra_pages: int = 0) -> Batch:
+    """The same batch (tokens, queries, scales) over a page table of 1-token
+    pages: every request's tokens get a page each, in a seeded random
+    permutation of the physical pages; the shared prefix tokens (if any) keep
+    shared pages, ids 0 .. S-1, first in every request's list."""
+    S = batch.cfg.shared_prefix_tokens
+    lens = [int(x) for x in batch.kv_lens]
+    n_private = sum(L - S for L in lens)
+    gen = torch.Generator().manual_seed(seed)
+    perm = torch.randperm(n_private, generator=gen) + S
+    idx, indptr, off = [], [0], 0
+    for L in lens:
+        idx.extend(range(S))
+        idx.extend(perm[off: off + L - S].tolist())
+        off += L - S
+        indptr.append(len(idx))
+    return dataclasses.replace(
+        batch, kv_indptr=torch.tensor(indptr, dtype=torch.int32),
+        kv_indices=torch.tensor(idx, dtype=torch.int32),
+        last_page_len=torch.ones(len(lens), dtype=torch.int32),
+        num_pages=S + n_private + extra_pages, page_size=1)

@@ -36,6 +36,7 @@ class GpuCase:
         if append:
             self.append(batch.prefix)
             self.append(batch.new)
+        plan_kw.setdefault("page_size", batch.page_size)
         self.plan = N.nvfp4kv_decode_plan(
             batch.qo_indptr, batch.kv_indptr, batch.last_page_len, c.num_qo_heads,
             c.num_kv_heads, c.head_dim_qk, c.head_dim_vo, causal=c.causal, **plan_kw)
@@ -53,8 +54,9 @@ class GpuCase:
         plan = plan or self.plan
         c = self.batch.cfg
         rows = int(self.batch.qo_indptr[-1])
+        dt = torch.float16 if plan.info.out_dtype == 1 else torch.bfloat16
         out = torch.full((rows, c.num_qo_heads, c.head_dim_vo), float("nan"),
-                         dtype=torch.bfloat16, device="cuda")
+                         dtype=dt, device="cuda")
         lse = torch.full((rows, c.num_qo_heads), float("nan"), device="cuda")
         N.nvfp4kv_decode_run(plan, self.q if q is None else q, self.cache, self.kv_indices,
                              self.batch.sm_scale, out=out, lse=lse)
@@ -98,10 +100,11 @@ def bf16_round(x: np.ndarray) -> np.ndarray:
     return torch.from_numpy(x).to(torch.bfloat16).double().numpy()
 
 
-def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
-    """Half a bf16 ulp at |x| (8 significant bits)."""
+def bf16_half_ulp(x: np.ndarray, mant_bits: int = 7) -> np.ndarray:
+    """Half an ulp at |x| of a format with mant_bits stored mantissa bits
+    (7: bf16, 10: f16)."""
     a = np.maximum(np.abs(x), 2.0 ** -126)
-    return 0.5 * 2.0 ** (np.floor(np.log2(a)) - 7)
+    return 0.5 * 2.0 ** (np.floor(np.log2(a)) - mant_bits)
 
 
 def compare(out_gpu, lse_gpu, out_orc, lse_orc, atol=OUT_ATOL, lse_atol=LSE_ATOL):
@@ -121,7 +124,8 @@ def compare(out_gpu, lse_gpu, out_orc, lse_orc, atol=OUT_ATOL, lse_atol=LSE_ATOL
     assert not np.isnan(lg[sel]).any(), "NaN in GPU lse"
     d = np.abs(og[sel] - out_orc[sel])
     dl = np.abs(lg[sel] - lse_orc[sel])
-    excess = d - bf16_half_ulp(np.maximum(np.abs(og[sel]), np.abs(out_orc[sel])))
+    mant = 10 if out_gpu.dtype == torch.float16 else 7
+    excess = d - bf16_half_ulp(np.maximum(np.abs(og[sel]), np.abs(out_orc[sel])), mant)
     ref = out_orc[sel].reshape(-1)
     got = og[sel].reshape(-1)
     stats = {

@@ -61,6 +61,7 @@ def check_cover(batch, p):
     u = units_of(p)
     c = batch.cfg
     kvp = batch.kv_indptr.tolist()
+    P = batch.page_size
     for b in range(c.batch):
         for h in range(c.num_kv_heads):
             sel = u[(u["b"] == b) & (u["h_kv"] == h)]
@@ -69,15 +70,16 @@ def check_cover(batch, p):
             pos = kvp[b]
             for k, x in enumerate(sel):
                 assert x["split"] == k and x["page_begin"] == pos
-                assert x["tok_begin"] == (pos - kvp[b]) * 16 and x["tok_begin"] % 16 == 0
+                assert x["tok_begin"] == (pos - kvp[b]) * P and x["tok_begin"] % 16 == 0
                 assert x["kv_len"] == batch.kv_lens[b]
                 pos += x["num_pages"]
             assert pos == kvp[b + 1]
     return u
 
 
+@pytest.mark.parametrize("page_size", [16, 1])
 @pytest.mark.parametrize("name", list(W.WORKLOADS))
-def test_plan_covers_all_pages(name):
+def test_plan_covers_all_pages(name, page_size):
     batch = W.make_batch(W.WORKLOADS[name]) if name != "prefix_cache_extend" else None
     if batch is None:  # the big extend batch: same page table, cheaper draw
         cfg = W.WORKLOADS[name]
@@ -85,7 +87,9 @@ def test_plan_covers_all_pages(name):
             kv_lens=[2000 + 997 * i for i in range(32)], qo_len=16, num_qo_heads=32,
             num_kv_heads=8, causal=True, shared_prefix_tokens=1024, seed=cfg.seed,
             batch=32))
-    p = plan(batch)
+    if page_size == 1:
+        batch = W.with_page_size_one(batch)
+    p = plan(batch, page_size=batch.page_size)
     u = check_cover(batch, p)
     i = p.info
     ctas = i.num_units * i.row_blocks
@@ -323,3 +327,31 @@ def test_dequantize_rejects_bad_arguments_and_accepts_empty():
     bad = fake_cache(page_size=8)
     assert L.nvfp4kv_dequantize_paged(C.byref(bad), buf, 4, buf, buf, None, None) == \
         _lib.ERR_UNSUPPORTED
+
+
+def test_plan_page_size_one_matches_sixteen():
+    """The same batch over 1-token pages plans the same units in tokens: the
+    unit token ranges, splits and kv lengths agree with the 16-token plan and
+    each unit holds 16 times the pages."""
+    batch = W.make_batch(W.WORKLOADS["batched_decode"])
+    b1 = W.with_page_size_one(batch)
+    p16, p1 = plan(batch), plan(b1, page_size=1)
+    u16, u1 = units_of(p16), units_of(p1)
+    assert p1.info.num_units == p16.info.num_units
+    for f in ("b", "h_kv", "tok_begin", "kv_len", "split", "num_splits", "partial_base"):
+        assert np.array_equal(u16[f], u1[f]), f
+    tok16 = np.minimum(u16["num_pages"] * 16, u16["kv_len"] - u16["tok_begin"])
+    assert np.array_equal(tok16, u1["num_pages"])
+    check_cover(b1, p1)
+
+
+def test_plan_rejects_other_page_sizes_and_dtypes():
+    batch = W.make_batch(W.WORKLOADS["tiny_decode"])
+    for ps in (8, 32, 0):
+        with pytest.raises(N.NvFp4KvError) as e:
+            plan(batch, page_size=ps)
+        assert e.value.status == _lib.ERR_UNSUPPORTED
+    with pytest.raises(ValueError):
+        plan(batch, out_dtype=torch.float32)
+    p = plan(batch, out_dtype=torch.float16)
+    assert p.info.out_dtype == 1
