@@ -57,9 +57,26 @@ constexpr int kTileTok = 128;
 constexpr int kThreads = 544;  // softmax warps 0-7, dequant warps 8-15, issue warp 16
 constexpr int kKB = 3;         // K_hat / V_hat buffers
 constexpr float kRaise = 8.f;  // log2 of the largest p before m is raised
-constexpr uint32_t kSleepNs = 20000;  // suspend hint of one poll
-constexpr uint32_t kPolls = 50000;    // polls before a wait gives up
-constexpr uint32_t kIdlePolls = 1u << 21;  // idle rounds of the product issuer
+// Wait bounds (the defaults give up after about a second; a test build
+// shortens them to about a millisecond).
+#ifndef NVFP4KV_TG5_SLEEP_NS
+#define NVFP4KV_TG5_SLEEP_NS 20000
+#endif
+#ifndef NVFP4KV_TG5_POLLS
+#define NVFP4KV_TG5_POLLS 50000
+#endif
+#ifndef NVFP4KV_TG5_IDLE_POLLS
+#define NVFP4KV_TG5_IDLE_POLLS (1u << 21)
+#endif
+// Test build only: the first dequant warp of CTA (0, 0) withholds its arrival
+// for the first tile, so the product issuer's bounded wait runs out and the
+// CTA takes the abort path (flag 0x4, every wait returns, the kernel ends).
+#ifndef NVFP4KV_TG5_TEST_SKIP_ARRIVE
+#define NVFP4KV_TG5_TEST_SKIP_ARRIVE 0
+#endif
+constexpr uint32_t kSleepNs = NVFP4KV_TG5_SLEEP_NS;  // suspend hint of one poll
+constexpr uint32_t kPolls = NVFP4KV_TG5_POLLS;       // polls before a wait gives up
+constexpr uint32_t kIdlePolls = NVFP4KV_TG5_IDLE_POLLS;  // idle rounds of the issuer
 
 // ---- tensor memory, tcgen05 and barrier helpers (inline PTX) -------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
@@ -474,7 +491,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&kv_full[bi]);
+      const bool withhold = NVFP4KV_TG5_TEST_SKIP_ARRIVE && blockIdx.x == 0 &&
+                            blockIdx.y == 0 && warp == 8 && i == 0;
+      if (lane == 0 && !withhold) mbar_arrive(&kv_full[bi]);
     }
     cp_async_wait<0>();
   } else if (warp == 16) {
