@@ -267,6 +267,12 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity, uint32
     if (mbar_try_wait_sleep(bar, parity)) return;
   atomicOr(flags, 0x4u);
 }
+// max of three floats in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 // order-preserving float <-> int keys (for integer max reductions)
 __device__ __forceinline__ int fkey(float f) {
   const int i = __float_as_int(f);
@@ -642,7 +648,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
     const bool active = c0 < nvalid;      // warp-uniform
 
     // x = log2-domain score relative to the running max, -inf where masked
-    auto scores = [&](int ch, int sb, bool tok_ok, bool mask_rows, int tok, float (&x)[CW]) {
+    // (a token past the unit's end gets garbage here: it is kept out of the
+    // raise test and its p is stored as 0)
+    auto scores = [&](int ch, int sb, bool mask_rows, int tok, float (&x)[CW]) {
       uint32_t sv[CW];
       tmem_ld<CW>(tmem + lane_base + T::SCOL + N * sb + c0 + ch * CW, sv);
       tmem_wait_ld<CW>(sv);
@@ -654,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
         const float ff[4] = {f.x, f.y, f.z, f.w}, nn[4] = {nm.x, nm.y, nm.z, nm.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          x[e4 + e] = tok_ok ? fmaf(__uint_as_float(sv[e4 + e]), ff[e], nn[e]) : -INFINITY;
+          x[e4 + e] = fmaf(__uint_as_float(sv[e4 + e]), ff[e], nn[e]);
         if (mask_rows) {
           const int4 lm = *reinterpret_cast<const int4*>(s_lim + cb + e4);
           const int ll[4] = {lm.x, lm.y, lm.z, lm.w};
@@ -694,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
           float xc[CW];
-          scores(ch, sb, tok_ok, mask_rows, tok, xc);
+          scores(ch, sb, mask_rows, tok, xc);
           if (unset) {
             const float4* th = reinterpret_cast<const float4*>(s_thr + c0 + ch * CW);
 #pragma unroll
@@ -708,11 +716,18 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
           for (int e = 0; e < CW; ++e) x[ch * CW + e] = xc[e];
         }
         if (!unset) {  // every real column has a maximum: one test of the largest
-          float mx = x[0];
+          float m3[(NH + 2) / 3];
 #pragma unroll
-          for (int e = 1; e < NH; ++e) mx = fmaxf(mx, x[e]);
+          for (int e = 0; e < NH / 3; ++e) m3[e] = fmax3(x[3 * e], x[3 * e + 1], x[3 * e + 2]);
+          if constexpr (NH % 3 == 1) m3[NH / 3] = x[NH - 1];
+          if constexpr (NH % 3 == 2) m3[NH / 3] = fmaxf(x[NH - 2], x[NH - 1]);
+          float mx = m3[0];
+#pragma unroll
+          for (int e = 1; e < (NH + 2) / 3; e += 2)
+            mx = e + 1 < (NH + 2) / 3 ? fmax3(mx, m3[e], m3[e + 1]) : fmaxf(mx, m3[e]);
           trig = mx > kRaise;
         }
+        trig = trig && tok_ok;
       }
       if (named_or(gbar, 128, trig)) {
         // ---- raise this half's running maxima to the tile's row maxima ----
@@ -721,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
         if (active) {
 #pragma unroll
           for (int e = 0; e < NH; ++e) {
-            const int k = __reduce_max_sync(0xffffffffu, fkey(x[e]));
+            const int k = __reduce_max_sync(0xffffffffu, fkey(tok_ok ? x[e] : -INFINITY));
             if (lane == 0) atomicMax(&s_max[c0 + e], k);
           }
         }
@@ -770,15 +785,24 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
       // ---- p = 2^x: the P^T row segment of this token --------------------
       if (active) {
         uint8_t* pt = sP + sb * T::PB;
-#pragma unroll
-        for (int c8 = 0; c8 < NH / 8; ++c8) {
-          uint32_t h[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            h[e] = f32x2_to_f16x2(ex2(x[8 * c8 + 2 * e]), ex2(x[8 * c8 + 2 * e + 1]));
+        auto pstore = [&](int c8, const uint32_t (&h)[4]) {
           const uint32_t off =
               (uint32_t)(j >> 3) * (8 * T::ROWB) + (j & 7) * T::ROWB + (c0 / 8 + c8) * 16;
           *reinterpret_cast<uint4*>(pt + swz<T::PSWB>(off)) = make_uint4(h[0], h[1], h[2], h[3]);
+        };
+        if (tok_ok) {
+#pragma unroll
+          for (int c8 = 0; c8 < NH / 8; ++c8) {
+            uint32_t h[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              h[e] = f32x2_to_f16x2(ex2(x[8 * c8 + 2 * e]), ex2(x[8 * c8 + 2 * e + 1]));
+            pstore(c8, h);
+          }
+        } else {  // a token past the unit's end: p = 0
+          const uint32_t z[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+          for (int c8 = 0; c8 < NH / 8; ++c8) pstore(c8, z);
         }
       }
       fence_async_smem();
