@@ -230,6 +230,9 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
   const uint8_t* sl = lane < SC ? ksb + lane * 16 : vsb + (lane - SC) * 16;
   const uint32_t slp = lane < SC ? kssp : vssp;
   const int soff = lane < SC ? T::OFF_KSF + lane * 16 : T::OFF_VSF + (lane - SC) * 16;
+  // shared addresses: this warp's stages, and this lane's copy targets in one
+  const uint32_t wpipe_s = smem_addr(wpipe);
+  const uint32_t lane_cp = wpipe_s + lane * 16, lane_sc = wpipe_s + soff;
   auto issue = [&](int j, int32_t pid) {
     uint8_t* st = wpipe + (j % STAGES) * T::STAGE_BYTES;
     if (lane == 0) sPid[warp * STAGES + j % STAGES] = pid;
@@ -244,14 +247,18 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
         bulk_g2s(st + T::OFF_VSF, vsb + (uint64_t)pg * vssp, T::VSF_BYTES, bar);
       }
     } else {
+      (void)st;
+      const uint32_t so = (j % STAGES) * T::STAGE_BYTES;
       const uint8_t* ks = kl + (uint64_t)pg * ksp;
       const uint8_t* vs = vl + (uint64_t)pg * vsp;
-#pragma unroll
-      for (int k = 0; k < KC; ++k) {
-        cp_async_16(st + lane * 16 + 512 * k, ks + 512 * k);
-        cp_async_16(st + T::OFF_V + lane * 16 + 512 * k, vs + 512 * k);
-      }
-      if (lane < 2 * SC) cp_async_16(st + soff, sl + (uint64_t)pg * slp);
+      static_assert(KC == 1 || KC == 2, "chunks per lane");
+      cp_async_16s<0>(lane_cp + so, ks);
+      if constexpr (KC == 2) cp_async_16s<512>(lane_cp + so, ks);
+      // V rows: the stage's V region starts OFF_V bytes in; the source
+      // offsets are those of the K copies
+      cp_async_16s<0>(lane_cp + so + T::OFF_V, vs);
+      if constexpr (KC == 2) cp_async_16s<512>(lane_cp + so + T::OFF_V, vs);
+      if (lane < 2 * SC) cp_async_16s<0>(lane_sc + so, sl + (uint64_t)pg * slp);
       cp_async_commit();
     }
   };
@@ -382,8 +389,18 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
 
   // rows of the page this lane reads: tokens of mma rows g, g+8 (K) and of
   // P columns 2t, 2t+1, 2t+8, 2t+9 (V)
-  const int kr0 = tok_of(g), kr1 = tok_of(g + 8);
-  const int vt[4] = {tok_of(2 * t), tok_of(2 * t + 1), tok_of(2 * t + 8), tok_of(2 * t + 9)};
+  // (tok_of(m + 8) = tok_of(m) + 8 and tok_of(2t + 1) = tok_of(2t) ^ 1, so
+  // the second row of each pair is an immediate 8 rows further on)
+  static_assert(T::NCH == 1, "one K chunk per lane");
+  const int kr0 = tok_of(g), vt0 = tok_of(2 * t), vt1 = vt0 ^ 1;
+  // byte offsets in a stage: K row kr0 at the lane's chunk t, its scale
+  // pair, V rows vt0 / vt1 at byte g VC, their scales at block g VC / 8
+  const uint32_t o_k = kr0 * T::KROW + t * T::CB;
+  const uint32_t o_ks = T::OFF_KSF + kr0 * T::KSFROW + t * (T::CB / 8);
+  const uint32_t o_v0 = T::OFF_V + vt0 * T::VROW + g * T::VC;
+  const uint32_t o_v1 = T::OFF_V + vt1 * T::VROW + g * T::VC;
+  const uint32_t o_vs0 = T::OFF_VSF + vt0 * T::VSFROW + (g * T::VC) / 8;
+  const uint32_t o_vs1 = T::OFF_VSF + vt1 * T::VSFROW + (g * T::VC) / 8;
   int fail_at = -1;
   for (int i = 0; i < npw; ++i) {
     const int j = i + STAGES - 1;
@@ -410,66 +427,59 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
       cp_async_wait<STAGES - 1>();
       __syncwarp();
     }
-    uint8_t* st = wpipe + (i % STAGES) * T::STAGE_BYTES;
+    const uint32_t so = (i % STAGES) * T::STAGE_BYTES;
     const int tok0 = u.tok_begin + (warp + i * WARPS) * 16;
-    const int valid = u.kv_len - tok0;  // tokens of this page that exist
-    if (new_lo < new_hi) patch_new(i, st, tok0);
+    if (new_lo < new_hi) patch_new(i, wpipe + so, tok0);
+    const uint32_t sb = wpipe_s + so;
 
-    // V rows and scales of this page
+    // V rows vt0, vt1, vt0 + 8, vt1 + 8 and their scales
     constexpr int VW = T::VC / 4 > 0 ? T::VC / 4 : 1;
+    constexpr int V8 = 8 * T::VROW, VS8 = 8 * T::VSFROW;
     uint32_t vw[4][VW];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint8_t* src = st + T::OFF_V + vt[k] * T::VROW + g * T::VC;
-      if constexpr (T::VC == 8) {
-        const uint2 v = *reinterpret_cast<const uint2*>(src);
-        vw[k][0] = v.x;
-        vw[k][1] = v.y;
-      } else {
-        vw[k][0] = *reinterpret_cast<const uint32_t*>(src);
-      }
+    if constexpr (T::VC == 8) {
+      const uint2 a = lds_v2<0>(sb + o_v0), b = lds_v2<0>(sb + o_v1);
+      const uint2 c2 = lds_v2<V8>(sb + o_v0), d = lds_v2<V8>(sb + o_v1);
+      vw[0][0] = a.x; vw[0][1] = a.y; vw[1][0] = b.x; vw[1][1] = b.y;
+      vw[2][0] = c2.x; vw[2][1] = c2.y; vw[3][0] = d.x; vw[3][1] = d.y;
+    } else {
+      vw[0][0] = lds_u32<0>(sb + o_v0);
+      vw[1][0] = lds_u32<0>(sb + o_v1);
+      vw[2][0] = lds_u32<V8>(sb + o_v0);
+      vw[3][0] = lds_u32<V8>(sb + o_v1);
     }
-    // slots past kv_len may hold a NaN scale byte: their V scale is forced to 0
-    uint32_t sA, sB;
-    {
-      const int blk = (g * T::VC * 2) / 16;
-      const uint8_t* sfs = st + T::OFF_VSF + blk;
-      uint32_t s0 = sfs[vt[0] * T::VSFROW], s1 = sfs[vt[1] * T::VSFROW];
-      uint32_t s2 = sfs[vt[2] * T::VSFROW], s3 = sfs[vt[3] * T::VSFROW];
-      if (valid < 16) {
-        if (vt[0] >= valid) s0 = 0;
-        if (vt[1] >= valid) s1 = 0;
-        if (vt[2] >= valid) s2 = 0;
-        if (vt[3] >= valid) s3 = 0;
-      }
-      sA = e4m3x2_to_f16x2(s0 | (s1 << 8));
-      sB = e4m3x2_to_f16x2(s2 | (s3 << 8));
+    uint32_t s0 = lds_u8<0>(sb + o_vs0), s1 = lds_u8<0>(sb + o_vs1);
+    uint32_t s2 = lds_u8<VS8>(sb + o_vs0), s3 = lds_u8<VS8>(sb + o_vs1);
+    const int valid = u.kv_len - tok0;  // tokens of this page that exist
+    if (valid < 16) {
+      // slots past kv_len may hold a NaN scale byte: their V scale is 0
+      if (vt0 >= valid) s0 = 0;
+      if (vt1 >= valid) s1 = 0;
+      if (vt0 + 8 >= valid) s2 = 0;
+      if (vt1 + 8 >= valid) s3 = 0;
     }
+    const uint32_t sA = e4m3x2_to_f16x2(__byte_perm(s0, s1, 0x1140));
+    const uint32_t sB = e4m3x2_to_f16x2(__byte_perm(s2, s3, 0x1140));
 
-    // ---- S^T = K_hat Q^T: mma rows g, g+8 = tokens kr0, kr1 -------------
-    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int cc = 0; cc < T::NCH; ++cc) {
-      const int ch = 4 * cc + t;
+    // ---- S^T = K_hat Q^T: mma rows g, g+8 = tokens kr0, kr0 + 8 ---------
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb4[4] = {0.f, 0.f, 0.f, 0.f};
+    constexpr int K8 = 8 * T::KROW, KS8 = 8 * T::KSFROW;
+    {
+      constexpr int cc = 0;
       uint32_t wg[T::CB / 4], w8[T::CB / 4], sg0, sg1, s80, s81;
       if constexpr (T::CB == 16) {
-        const uint4 a = *reinterpret_cast<const uint4*>(st + kr0 * T::KROW + ch * 16);
-        const uint4 b = *reinterpret_cast<const uint4*>(st + kr1 * T::KROW + ch * 16);
+        const uint4 a = lds_v4<0>(sb + o_k), b = lds_v4<K8>(sb + o_k);
         wg[0] = a.x; wg[1] = a.y; wg[2] = a.z; wg[3] = a.w;
         w8[0] = b.x; w8[1] = b.y; w8[2] = b.z; w8[3] = b.w;
-        const uint32_t ga = e4m3x2_to_f16x2(
-            *reinterpret_cast<const uint16_t*>(st + T::OFF_KSF + kr0 * T::KSFROW + 2 * ch));
-        const uint32_t gb = e4m3x2_to_f16x2(
-            *reinterpret_cast<const uint16_t*>(st + T::OFF_KSF + kr1 * T::KSFROW + 2 * ch));
+        const uint32_t ga = e4m3x2_to_f16x2(lds_u16<0>(sb + o_ks));
+        const uint32_t gb = e4m3x2_to_f16x2(lds_u16<KS8>(sb + o_ks));
         sg0 = bcast_lo(ga); sg1 = bcast_hi(ga);
         s80 = bcast_lo(gb); s81 = bcast_hi(gb);
       } else {
-        const uint2 a = *reinterpret_cast<const uint2*>(st + kr0 * T::KROW + ch * 8);
-        const uint2 b = *reinterpret_cast<const uint2*>(st + kr1 * T::KROW + ch * 8);
+        const uint2 a = lds_v2<0>(sb + o_k), b = lds_v2<K8>(sb + o_k);
         wg[0] = a.x; wg[1] = a.y;
         w8[0] = b.x; w8[1] = b.y;
-        sg0 = sg1 = bcast_lo(e4m3x2_to_f16x2(st[T::OFF_KSF + kr0 * T::KSFROW + ch]));
-        s80 = s81 = bcast_lo(e4m3x2_to_f16x2(st[T::OFF_KSF + kr1 * T::KSFROW + ch]));
+        sg0 = sg1 = bcast_lo(e4m3x2_to_f16x2(lds_u8<0>(sb + o_ks)));
+        s80 = s81 = bcast_lo(e4m3x2_to_f16x2(lds_u8<KS8>(sb + o_ks)));
       }
 #pragma unroll
       for (int q = 0; q < T::CB / 4; ++q) {
@@ -486,7 +496,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
         const uint32_t a0[4] = {hg[0], h8[0], hg[1], h8[1]};
         const uint32_t a1[4] = {hg[2], h8[2], hg[3], h8[3]};
         mma_16816(sa, a0, qreg[kk][0], qreg[kk][1]);
-        mma_16816(sb, a1, qreg[kk + 1][0], qreg[kk + 1][1]);
+        mma_16816(sb4, a1, qreg[kk + 1][0], qreg[kk + 1][1]);
       }
     }
 
@@ -494,16 +504,16 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
     // x[0..3] = tokens kr0, kr0, kr1, kr1 x rows 2t, 2t+1, 2t, 2t+1
     float x[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) x[k] = fmaf(sa[k] + sb[k], f2[k & 1], nm2[k & 1]);
+    for (int k = 0; k < 4; ++k) x[k] = fmaf(sa[k] + sb4[k], f2[k & 1], nm2[k & 1]);
     if (tok0 + 15 > min_lim) {
-      const int ta = tok0 + kr0, tb = tok0 + kr1;
+      const int ta = tok0 + kr0, tb = ta + 8;
       if (ta > lim2[0]) x[0] = -INFINITY;
       if (ta > lim2[1]) x[1] = -INFINITY;
       if (tb > lim2[0]) x[2] = -INFINITY;
       if (tb > lim2[1]) x[3] = -INFINITY;
     }
     const bool trig = fmaxf(x[0], x[2]) > thr2[0] || fmaxf(x[1], x[3]) > thr2[1];
-    if (__any_sync(0xffffffffu, trig)) {
+    if (__builtin_expect(__any_sync(0xffffffffu, trig), 0)) {
       // raise each row's maximum to this page's exact maximum (a row's
       // values sit in the 8 lanes of the same t)
       float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};

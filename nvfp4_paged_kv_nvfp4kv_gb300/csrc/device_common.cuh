@@ -39,6 +39,46 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
+// Loads from a 32-bit shared-memory address plus a compile-time byte offset
+// (volatile: they stay after the waits and barriers that precede them).
+template <int OFF = 0>
+__device__ __forceinline__ uint32_t lds_u8(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1+%2];\n" : "=r"(v) : "r"(a), "n"(OFF));
+  return v;
+}
+template <int OFF = 0>
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u16 %0, [%1+%2];\n" : "=r"(v) : "r"(a), "n"(OFF));
+  return v;
+}
+template <int OFF = 0>
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1+%2];\n" : "=r"(v) : "r"(a), "n"(OFF));
+  return v;
+}
+template <int OFF = 0>
+__device__ __forceinline__ uint2 lds_v2(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2+%3];\n" : "=r"(v.x), "=r"(v.y) : "r"(a), "n"(OFF));
+  return v;
+}
+template <int OFF = 0>
+__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4+%5];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a), "n"(OFF));
+  return v;
+}
+// 16-byte cp.async to a 32-bit shared address (both addresses plus OFF)
+template <int OFF = 0>
+__device__ __forceinline__ void cp_async_16s(uint32_t s, const void* g) {
+  asm volatile("cp.async.cg.shared.global [%0+%2], [%1+%2], 16;\n" ::"r"(s), "l"(g), "n"(OFF));
+}
+
 // ---- mbarrier ----
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_addr(bar)), "r"(count));
