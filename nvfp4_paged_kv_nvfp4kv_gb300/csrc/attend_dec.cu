@@ -48,6 +48,12 @@ constexpr uint32_t kDecHintNs = 100000;         // suspend hint of one poll
 constexpr uint64_t kDecWaitNs = 2000000000ull;  // a stage wait gives up after 2 s
 constexpr float kDecRaiseLog2 = 8.f;
 
+// 1: the lean part of the page loop is unrolled by the ring depth, so the
+// stage offsets are immediates
+#ifndef NVFP4KV_DEC_UNROLL
+#define NVFP4KV_DEC_UNROLL 1
+#endif
+
 template <int DK, int DV, int WARPS, int STAGES>
 struct DecTraits {
   static constexpr int KROW = DK / 2, VROW = DV / 2, KSFROW = DK / 16, VSFROW = DV / 16;
@@ -119,6 +125,12 @@ __device__ __forceinline__ bool dec_wait(uint64_t* bar, uint32_t parity) {
   while (!mbar_wait_hint(bar, parity, kDecHintNs))
     if (global_ns() - t0 > kDecWaitNs) return false;
   return true;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 // token of mma row / P column m of a page
@@ -233,9 +245,10 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
   // shared addresses: this warp's stages, and this lane's copy targets in one
   const uint32_t wpipe_s = smem_addr(wpipe);
   const uint32_t lane_cp = wpipe_s + lane * 16, lane_sc = wpipe_s + soff;
-  auto issue = [&](int j, int32_t pid) {
-    uint8_t* st = wpipe + (j % STAGES) * T::STAGE_BYTES;
-    if (lane == 0) sPid[warp * STAGES + j % STAGES] = pid;
+  // page j into stage js (= j % STAGES)
+  auto issue = [&](int j, int32_t pid, int js) {
+    uint8_t* st = wpipe + js * T::STAGE_BYTES;
+    if (lane == 0) sPid[warp * STAGES + js] = pid;
     const uint32_t pg = (uint32_t)max(pid, 0);
     if constexpr (BULK) {
       if (lane == 0) {
@@ -248,16 +261,15 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
       }
     } else {
       (void)st;
-      const uint32_t so = (j % STAGES) * T::STAGE_BYTES;
+      const uint32_t so = js * T::STAGE_BYTES;
       const uint8_t* ks = kl + (uint64_t)pg * ksp;
       const uint8_t* vs = vl + (uint64_t)pg * vsp;
       static_assert(KC == 1 || KC == 2, "chunks per lane");
       cp_async_16s<0>(lane_cp + so, ks);
       if constexpr (KC == 2) cp_async_16s<512>(lane_cp + so, ks);
-      // V rows: the stage's V region starts OFF_V bytes in; the source
-      // offsets are those of the K copies
-      cp_async_16s<0>(lane_cp + so + T::OFF_V, vs);
-      if constexpr (KC == 2) cp_async_16s<512>(lane_cp + so + T::OFF_V, vs);
+      // V rows: the stage's V region starts OFF_V bytes in
+      cp_async_16s<T::OFF_V, 0>(lane_cp + so, vs);
+      if constexpr (KC == 2) cp_async_16s<T::OFF_V + 512, 512>(lane_cp + so, vs);
       if (lane < 2 * SC) cp_async_16s<0>(lane_sc + so, sl + (uint64_t)pg * slp);
       cp_async_commit();
     }
@@ -265,7 +277,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
 #pragma unroll
   for (int j = 0; j < STAGES - 1; ++j) {
     const int32_t pid = __shfl_sync(0xffffffffu, ids_cur, j);
-    if (j < npw) issue(j, pid);
+    if (j < npw) issue(j, pid, j);
     else if constexpr (!BULK) cp_async_commit();
   }
 
@@ -319,7 +331,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
   // this lane's query rows 2t and 2t+1: score factor f, -m_use, raise
   // threshold (-inf until the row has a maximum, +inf for padding rows),
   // causal limit, running max (log2) and partial sum
-  float f2[2], nm2[2], thr2[2], mrow[2], lrow[2];
+  float f2[2], nm2[2], thr2[2], mrow[2], lrow[2], thr_lane;
   int lim2[2];
   int min_lim = INT32_MAX;
   for (int rr = 0; rr < T::RB; ++rr)
@@ -333,6 +345,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
     mrow[k] = -INFINITY;
     lrow[k] = 0.f;
   }
+  thr_lane = fminf(thr2[0], thr2[1]);
   // Q fragments (the B operand of S^T): k-step kk covers the 4 dims at
   // 2 (4c + t) CB + 4m for chunk c = kk / KS_PER_CH, step m
   uint32_t qreg[T::KSTEPS][2];
@@ -401,15 +414,31 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
   const uint32_t o_v1 = T::OFF_V + vt1 * T::VROW + g * T::VC;
   const uint32_t o_vs0 = T::OFF_VSF + vt0 * T::VSFROW + (g * T::VC) / 8;
   const uint32_t o_vs1 = T::OFF_VSF + vt1 * T::VSFROW + (g * T::VC) / 8;
+  // Pages whose tokens reach the smallest row limit need the causal /
+  // length mask, and pages holding this step's new tokens need the patch:
+  // both sit at the end of the unit, so the loop runs a lean body over the
+  // pages before the first such page and the full body over the rest.
+  int tail_tok = min_lim;  // a page is special once tok0 + 15 > tail_tok
+  if (new_lo < new_hi) tail_tok = min(tail_tok, new_lo - 1);
+  int n_lean = 0;          // this warp's pages before the first special one
+  {
+    const int ok = tail_tok - 15 - u.tok_begin;  // pages pi with 16 pi <= ok
+    const int unit_ok = ok >= 0 ? ok / 16 + 1 : 0;
+    n_lean = unit_ok > warp ? min(npw, (unit_ok - warp + WARPS - 1) / WARPS) : 0;
+  }
   int fail_at = -1;
-  for (int i = 0; i < npw; ++i) {
+  // one page; false when its copy wait ran out
+  // page i, held in stage is (= i % STAGES: a constant where the caller
+  // unrolls, so the stage offsets become immediates)
+  auto page = [&](int i, auto special, int is) -> bool {
+    constexpr bool SP = decltype(special)::value;
     const int j = i + STAGES - 1;
     if (j < npw) {
       if ((j & 31) == 0) {
         ids_cur = ids_nxt;
         ids_nxt = load_ids(j / 32 + 1);
       }
-      issue(j, __shfl_sync(0xffffffffu, ids_cur, j & 31));
+      issue(j, __shfl_sync(0xffffffffu, ids_cur, j & 31), (is + STAGES - 1) % STAGES);
     } else if constexpr (!BULK) {
       cp_async_commit();  // keep one group per page for the wait count
     }
@@ -421,15 +450,17 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
       if (!landed) {
         if (lane == 0) atomicOr(p.flags, 0x4u);
         fail_at = i;
-        break;
+        return false;
       }
     } else {
       cp_async_wait<STAGES - 1>();
       __syncwarp();
     }
-    const uint32_t so = (i % STAGES) * T::STAGE_BYTES;
+    const uint32_t so = is * T::STAGE_BYTES;
     const int tok0 = u.tok_begin + (warp + i * WARPS) * 16;
-    if (new_lo < new_hi) patch_new(i, wpipe + so, tok0);
+    if constexpr (SP) {
+      if (new_lo < new_hi) patch_new(i, wpipe + so, tok0);
+    }
     const uint32_t sb = wpipe_s + so;
 
     // V rows vt0, vt1, vt0 + 8, vt1 + 8 and their scales
@@ -450,7 +481,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
     uint32_t s0 = lds_u8<0>(sb + o_vs0), s1 = lds_u8<0>(sb + o_vs1);
     uint32_t s2 = lds_u8<VS8>(sb + o_vs0), s3 = lds_u8<VS8>(sb + o_vs1);
     const int valid = u.kv_len - tok0;  // tokens of this page that exist
-    if (valid < 16) {
+    if (SP && valid < 16) {
       // slots past kv_len may hold a NaN scale byte: their V scale is 0
       if (vt0 >= valid) s0 = 0;
       if (vt1 >= valid) s1 = 0;
@@ -505,14 +536,16 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
     float x[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) x[k] = fmaf(sa[k] + sb4[k], f2[k & 1], nm2[k & 1]);
-    if (tok0 + 15 > min_lim) {
+    if (SP && tok0 + 15 > min_lim) {
       const int ta = tok0 + kr0, tb = ta + 8;
       if (ta > lim2[0]) x[0] = -INFINITY;
       if (ta > lim2[1]) x[1] = -INFINITY;
       if (tb > lim2[0]) x[2] = -INFINITY;
       if (tb > lim2[1]) x[3] = -INFINITY;
     }
-    const bool trig = fmaxf(x[0], x[2]) > thr2[0] || fmaxf(x[1], x[3]) > thr2[1];
+    // raise test against the lane's smaller threshold (a superset of the
+    // rows that need it: the raise itself works per row)
+    const bool trig = fmax3(x[0], x[1], fmaxf(x[2], x[3])) > thr_lane;
     if (__builtin_expect(__any_sync(0xffffffffu, trig), 0)) {
       // raise each row's maximum to this page's exact maximum (a row's
       // values sit in the 8 lanes of the same t)
@@ -530,6 +563,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
           mrow[k] = (mrow[k] == -INFINITY ? 0.f : mrow[k]) + mx[k];
           nm2[k] = -mrow[k];
           thr2[k] = kDecRaiseLog2;
+          thr_lane = fminf(thr2[0], thr2[1]);
           x[k] -= mx[k];
           x[k + 2] -= mx[k];
         }
@@ -582,6 +616,23 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
       }
     }
     __syncwarp();  // every lane has read the stage before lane 0 refills it
+    return true;
+  };
+  {
+    int i = 0;
+#if NVFP4KV_DEC_UNROLL
+    for (; fail_at < 0 && i + STAGES <= n_lean; i += STAGES) {
+#pragma unroll
+      for (int k = 0; k < STAGES; ++k)
+        if (fail_at < 0) page(i + k, std::false_type{}, k);
+    }
+#endif
+    if (fail_at < 0)
+      for (; i < n_lean; ++i)
+        if (!page(i, std::false_type{}, i % STAGES)) break;
+    if (fail_at < 0)
+      for (; i < npw; ++i)
+        if (!page(i, std::true_type{}, i % STAGES)) break;
   }
   if constexpr (!BULK) cp_async_wait<0>();
   if (fail_at >= 0) {

@@ -73,10 +73,12 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t a) {
                : "r"(a), "n"(OFF));
   return v;
 }
-// 16-byte cp.async to a 32-bit shared address (both addresses plus OFF)
-template <int OFF = 0>
+// 16-byte cp.async to a 32-bit shared address: shared s + SOFF <- global
+// g + GOFF
+template <int SOFF = 0, int GOFF = SOFF>
 __device__ __forceinline__ void cp_async_16s(uint32_t s, const void* g) {
-  asm volatile("cp.async.cg.shared.global [%0+%2], [%1+%2], 16;\n" ::"r"(s), "l"(g), "n"(OFF));
+  asm volatile("cp.async.cg.shared.global [%0+%2], [%1+%3], 16;\n" ::"r"(s), "l"(g), "n"(SOFF),
+               "n"(GOFF));
 }
 
 // ---- mbarrier ----
