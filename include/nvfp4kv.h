@@ -76,6 +76,9 @@ typedef enum nvfp4kv_status {
 #define NVFP4KV_FLAG_BAD_LIVE_LENGTH 0x8u /* a live last_page_len was outside
                                            [1, 16] or left fewer tokens than
                                            query rows (clamped)              */
+#define NVFP4KV_FLAG_PACE_TIMEOUT 0x10u /* a pacing wait between the units of
+                                           a decode CTA ran out; pacing
+                                           carries no data, results stand  */
 
 const char* nvfp4kv_status_string(int status);
 const char* nvfp4kv_last_error_detail(void);

@@ -26,6 +26,7 @@ FLAG_BAD_PAGE_INDEX = 0x1
 FLAG_BAD_APPEND_TARGET = 0x2
 FLAG_COPY_TIMEOUT = 0x4
 FLAG_BAD_LIVE_LENGTH = 0x8
+FLAG_PACE_TIMEOUT = 0x10
 
 
 class PagedCacheStruct(C.Structure):

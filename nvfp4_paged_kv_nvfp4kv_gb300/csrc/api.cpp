@@ -21,7 +21,7 @@ namespace nvfp4kv {
 bool attend_config_tc(int dk, int dv, int rows, AttendConfig* cfg);
 bool attend_config_simt(int dk, int dv, int rows, AttendConfig* cfg);
 bool attend_config_tcgen05(int dk, int dv, int rows, AttendConfig* cfg);
-bool attend_config_dec(int dk, int dv, int rows, AttendConfig* cfg);
+bool attend_config_dec(int dk, int dv, int rows, int quads, AttendConfig* cfg);
 cudaError_t prepare_kernel(const AttendConfig& cfg);
 }  // namespace nvfp4kv
 
@@ -359,6 +359,19 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
                                           : "CUDA-core",
                 head_dim_qk, head_dim_vo);
   const int rows_per_block = cfg.rows;
+  // A tensor-core plan of one block of <= 8 rows at page size 16 runs the
+  // decode kernel where the cache layout allows it; that kernel takes several
+  // units per CTA, so its occupancy (in units) sizes the wave.
+  AttendConfig occ = cfg;
+  int units_per_cta = 1;
+  {
+    AttendConfig dcfg{};
+    if (kind == kKernelTensorCore && rows_per_block == 8 && page_size == kPageSize &&
+        attend_config_dec(head_dim_qk, head_dim_vo, 8, 4, &dcfg)) {
+      occ = dcfg;
+      units_per_cta = std::max(1, dcfg.units_per_cta);
+    }
+  }
   int num_sms = opts.num_sms, ctas_per_sm = opts.ctas_per_sm;
   if (num_sms == 0 || ctas_per_sm == 0) {
     int dev = device;
@@ -373,7 +386,7 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
     std::pair<int, int> sm_occ{0, 0};
     {
       std::lock_guard<std::mutex> lock(mu);
-      auto it = known.find({dev, cfg.func});
+      auto it = known.find({dev, occ.func});
       if (it != known.end()) sm_occ = it->second;
     }
     if (sm_occ.first == 0) {
@@ -382,23 +395,24 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
       int optin = 0;
       e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
       if (e != cudaSuccess) return cuda_fail(e, "shared-memory opt-in");
-      if (cfg.smem_bytes > optin)
+      if (occ.smem_bytes > optin)
         return fail(NVFP4KV_ERR_UNSUPPORTED,
                     "kernel needs %d bytes of shared memory, device allows %d per block",
-                    cfg.smem_bytes, optin);
+                    occ.smem_bytes, optin);
       int cur = -1;
       e = cudaGetDevice(&cur);
       if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
       if (cur != dev && (e = cudaSetDevice(dev)) != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
-      e = prepare_kernel(cfg);
+      e = prepare_kernel(occ);
       if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sm_occ.second, cfg.func,
-                                                          cfg.warps * 32, cfg.smem_bytes);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sm_occ.second, occ.func,
+                                                          occ.warps * 32, occ.smem_bytes);
       if (cur != dev) cudaSetDevice(cur);
       if (e != cudaSuccess) return cuda_fail(e, "occupancy");
       if (sm_occ.second < 1) sm_occ.second = 1;
+      sm_occ.second *= units_per_cta;  // unit slots per SM
       std::lock_guard<std::mutex> lock(mu);
-      known[{dev, cfg.func}] = sm_occ;
+      known[{dev, occ.func}] = sm_occ;
     }
     if (num_sms == 0) num_sms = sm_occ.first;
     if (ctas_per_sm == 0) ctas_per_sm = sm_occ.second;
@@ -654,7 +668,8 @@ int attend(const nvfp4kv_plan_info* info, const void* q_bf16, int64_t q_stride_t
   // or better: the plan's one-wave grid stays one wave)
   const bool dec = info->kernel == kKernelTensorCore && info->rows_per_block == 8 &&
                    info->page_size == kPageSize && bulk_decode_layout(cache) &&
-                   attend_config_dec(info->head_dim_qk, info->head_dim_vo, 8, &cfg);
+                   attend_config_dec(info->head_dim_qk, info->head_dim_vo, 8,
+                                     info->num_units <= info->num_sms ? 1 : 4, &cfg);
   if (!dec && !lookup_kernel(info->kernel, info->head_dim_qk, info->head_dim_vo,
                              info->rows_per_block, &cfg))
     return fail(NVFP4KV_ERR_UNSUPPORTED, "planned kernel not available");
@@ -669,6 +684,7 @@ int attend(const nvfp4kv_plan_info* info, const void* q_bf16, int64_t q_stride_t
   p.cache = view_of(cache);
   p.kv_indices = kv_indices;
   p.units = reinterpret_cast<const WorkUnit*>(ws + info->off_units);
+  p.num_units = info->num_units;
   p.num_qo_heads = info->num_qo_heads;
   p.group = info->num_qo_heads / info->num_kv_heads;
   p.causal = info->causal;

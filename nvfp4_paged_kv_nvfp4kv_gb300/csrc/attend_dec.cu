@@ -11,9 +11,13 @@
 //  * Each warp owns every WARPS-th page of the work unit.  Its page ids sit in
 //    one register (lane k holds the id of its page 32 b + k), read 32 pages
 //    ahead and checked against the pool once; a page's id comes from a shuffle.
-//  * One lane copies a page with four bulk copies (packed K rows, packed V
-//    rows, K scales, V scales: one contiguous region each in an HND cache)
-//    that complete on the stage's mbarrier; every wait is bounded.
+//  * Every lane copies 16-byte pieces of a page (packed K rows, packed V rows,
+//    the two scale regions) with cp.async into a ring of STAGES stages per
+//    warp, one commit group per page.
+//  * A CTA holds four such units (16 warps).  The warp schedulers favour the
+//    oldest warps, so separate CTAs of one SM finish their equal shares at
+//    very different times; the four units of a CTA instead meet at a
+//    CTA-wide barrier after every round of STAGES pages and stay level.
 //  * Tokens of a page are taken in the order m -> m ^ ((m >> 1) & 1) for the
 //    rows of the score product, the columns of P and the rows of V alike (a
 //    contraction does not depend on the order of its terms), so the lanes'
@@ -44,15 +48,25 @@ namespace {
 
 using namespace dev;
 
-constexpr uint32_t kDecHintNs = 100000;         // suspend hint of one poll
-constexpr uint64_t kDecWaitNs = 2000000000ull;  // a stage wait gives up after 2 s
 constexpr float kDecRaiseLog2 = 8.f;
+constexpr uint32_t kPaceHintNs = 2000;  // suspend hint of one pacing poll
+constexpr int kPacePolls = 5000;        // a pacing wait gives up after these polls
 
-// 1: the lean part of the page loop is unrolled by the ring depth, so the
-// stage offsets are immediates
-#ifndef NVFP4KV_DEC_UNROLL
-#define NVFP4KV_DEC_UNROLL 1
-#endif
+// One poll of an mbarrier phase that may suspend the thread until the phase
+// completes or about `ns` nanoseconds pass.
+__device__ __forceinline__ bool mbar_wait_hint(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void mbar_arrive_one(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_addr(bar)) : "memory");
+}
 
 template <int DK, int DV, int WARPS, int STAGES>
 struct DecTraits {
@@ -76,56 +90,16 @@ struct DecTraits {
   static constexpr int OFF_Q = MAIN_BYTES;
   static constexpr int OFF_ROW = OFF_Q + Q_BYTES;      // RB floats + RB ints; later
   static constexpr int ROW_BYTES = 2 * RB * 4 + 16;    // the epilogue's 2 RB + 1 words
-  static constexpr int OFF_BAR = (OFF_ROW + ROW_BYTES + 7) / 8 * 8;
-  static constexpr int OFF_PID = OFF_BAR + WARPS * STAGES * 8;  // page id of each stage
-  static constexpr int NEW_ROW = (DK + DV) * 2;        // bf16 K and V of one new token
+  // bf16 K and V rows of the fused append's new tokens (at most RB per unit)
+  static constexpr int NEW_ROW = (DK + DV) * 2;
+  static constexpr int OFF_PID = (OFF_ROW + ROW_BYTES + 15) / 16 * 16;  // page id per stage
   static constexpr int OFF_NEW = (OFF_PID + WARPS * STAGES * 4 + 15) / 16 * 16;
-  static constexpr int SMEM = OFF_NEW + RB * NEW_ROW;  // at most RB new tokens per unit
+  static constexpr int SMEM = OFF_NEW + RB * NEW_ROW;
+  static constexpr int SMEM_Q = (SMEM + 127) / 128 * 128;  // one quad's share of the CTA
   static_assert(DK <= 128 && DV <= 128 && DK % 64 == 0 && DV % 64 == 0, "head dims");
   static_assert(K_BYTES % 16 == 0 && V_BYTES % 16 == 0 && KSF_BYTES % 16 == 0 &&
                     VSF_BYTES % 16 == 0 && STAGE_BYTES % 16 == 0, "bulk copy sizes");
 };
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_addr(bar)),
-               "r"(bytes)
-               : "memory");
-}
-// global -> shared bulk copy completing `bytes` of the mbarrier's transaction
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
-                                         uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
-          smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %globaltimer;\n" : "=l"(t));
-  return t;
-}
-// One poll that may suspend the thread until the phase completes or the
-// hinted time (ns) passes.
-__device__ __forceinline__ bool mbar_wait_hint(uint64_t* bar, uint32_t parity, uint32_t ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait for a stage, by one lane (the others sleep in __syncwarp):
-// false once kDecWaitNs of wall time have passed without completion.
-__device__ __forceinline__ bool dec_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_wait_hint(bar, parity, kDecHintNs)) return true;
-  const uint64_t t0 = global_ns();
-  while (!mbar_wait_hint(bar, parity, kDecHintNs))
-    if (global_ns() - t0 > kDecWaitNs) return false;
-  return true;
-}
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
@@ -136,28 +110,48 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // token of mma row / P column m of a page
 __device__ __forceinline__ int tok_of(int m) { return m ^ ((m >> 1) & 1); }
 
-template <int DK, int DV, int WARPS, int STAGES, bool BULK>
-__global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendParams p) {
+// QUADS groups of WARPS warps per CTA, one work unit each (unit
+// QUADS * blockIdx.x + quad).  The groups share nothing but the CTA: each
+// synchronises on its own named barrier.  Their pages go in rounds of STAGES
+// per warp, and no warp starts a round before every warp of the CTA has
+// finished the round before the previous one (two mbarriers, one per round
+// parity), so the units of an SM advance together instead of in the order
+// the warp schedulers favour.  The pacing carries no data: a pacing wait
+// that runs out sets NVFP4KV_FLAG_PACE_TIMEOUT and the warp goes on.
+template <int DK, int DV, int WARPS, int STAGES, int QUADS>
+__global__ void __launch_bounds__(WARPS * 32 * QUADS, 1) attend_dec_kernel(const AttendParams p) {
   using T = DecTraits<DK, DV, WARPS, STAGES>;
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem_all[];
+  const int quad = threadIdx.x / (WARPS * 32);
+  const int unit = blockIdx.x * QUADS + quad;
+  int* s_rounds = reinterpret_cast<int*>(smem_all + QUADS * T::SMEM_Q);
+  uint64_t* s_pace = reinterpret_cast<uint64_t*>(smem_all + QUADS * T::SMEM_Q + 8);
+  if (threadIdx.x == 0) {
+    *s_rounds = 0;
+    const int live = min(QUADS, p.num_units - (int)blockIdx.x * QUADS);
+    mbar_init(&s_pace[0], live * WARPS);  // one arrival per warp of a unit
+    mbar_init(&s_pace[1], live * WARPS);
+  }
+  __syncthreads();  // (CTA-wide 1 of 2)
+  if (unit >= p.num_units) {
+    __syncthreads();  // (CTA-wide 2 of 2); no unit for this group
+    return;
+  }
+  auto qsync = [quad] {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(1 + quad), "n"(WARPS * 32) : "memory");
+  };
+  uint8_t* smem = smem_all + quad * T::SMEM_Q;
   uint8_t* pipe = smem;
   uint16_t* sQ = reinterpret_cast<uint16_t*>(smem + T::OFF_Q);
   float* sRowF = reinterpret_cast<float*>(smem + T::OFF_ROW);
   int* sRowLim = reinterpret_cast<int*>(sRowF + T::RB);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
   int32_t* sPid = reinterpret_cast<int32_t*>(smem + T::OFF_PID);
   uint8_t* sNew = smem + T::OFF_NEW;
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x % (WARPS * 32), lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
-  uint64_t* wbar = bars + warp * STAGES;
-  if (lane == 0) {
-#pragma unroll
-    for (int s = 0; s < STAGES; ++s) mbar_init(&wbar[s], 1);
-    mbar_init_fence();
-  }
 
-  const WorkUnit u = load_unit(p);
+  const WorkUnit u = load_unit(p, unit, tid == 0);
   const int G = p.group;
   const int R = G * u.qo_len;   // <= 8: one row block
   const int npw = u.num_pages > warp ? (u.num_pages - warp + WARPS - 1) / WARPS : 0;
@@ -180,6 +174,34 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
   int32_t ids_cur = load_ids(0);
   int32_t ids_nxt = npw > 32 ? load_ids(1) : 0;
 
+  // ---- fused append: this kv head's new tokens in the unit's pages --------
+  // [new_lo, new_hi): positions of the step's new tokens in this unit.  The
+  // warp that streams a token's page prefetches its bf16 K and V rows into
+  // sNew (cp.async, with its first page) and, when the page has landed,
+  // quantises them (the recipe of quantize_append) into the cache for later
+  // steps and into the stage (its copy may have read the page before the
+  // cache store).  A page belongs to one warp, so no other warp or CTA reads
+  // the stored bytes in this launch.
+  const int first_new = u.kv_len - u.qo_len;
+  int new_lo = 0, new_hi = 0;
+  if (p.new_k != nullptr) {
+    new_lo = max(first_new, u.tok_begin);
+    new_hi = min(u.kv_len, u.tok_begin + 16 * u.num_pages);
+  }
+  {
+    constexpr int NCK = T::NEW_ROW / 16;  // 16-byte chunks of one new token
+    for (int idx = lane; idx < (new_hi - new_lo) * NCK; idx += 32) {
+      const int tok = new_lo + idx / NCK, ch = idx % NCK;
+      if (((tok - u.tok_begin) / 16) % WARPS != warp) continue;
+      const int i = tok - first_new;
+      const uint16_t* src =
+          ch < DK / 8 ? p.new_k + (int64_t)(u.qo_begin + i) * p.nk_stride_tok +
+                            (int64_t)u.h_kv * p.nk_stride_head + 8 * ch
+                      : p.new_v + (int64_t)(u.qo_begin + i) * p.nv_stride_tok +
+                            (int64_t)u.h_kv * p.nv_stride_head + 8 * (ch - DK / 8);
+      cp_async_16(sNew + (tok - new_lo) * T::NEW_ROW + 16 * ch, src);
+    }
+  }
   // ---- Q rows: one 16-byte load per thread per 8 elements ----------------
   constexpr int QCH = T::RB * DK / 8;
   constexpr int QPT = (QCH + WARPS * 32 - 1) / (WARPS * 32);
@@ -198,29 +220,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
   }
   if (tid < T::RB) reinterpret_cast<int*>(sRowF)[tid] = 0;  // per-row amax bits
 
-  // ---- fused append: this kv head's new tokens in the unit's pages --------
-  // [new_lo, new_hi): positions of the step's new tokens in this unit; the
-  // warp owning a token's page prefetches its bf16 K and V rows into sNew
-  // (cp.async, in the group of its first page)
-  const int first_new = u.kv_len - u.qo_len;
-  int new_lo = 0, new_hi = 0;
-  if (p.new_k != nullptr) {
-    new_lo = max(first_new, u.tok_begin);
-    new_hi = min(u.kv_len, u.tok_begin + 16 * u.num_pages);
-  }
-  constexpr int NCK = T::NEW_ROW / 16;  // 16-byte chunks of one new token
-  for (int idx = lane; idx < (new_hi - new_lo) * NCK; idx += 32) {
-    const int tok = new_lo + idx / NCK, ch = idx % NCK;
-    if (((tok - u.tok_begin) / 16) % WARPS != warp) continue;
-    const int i = tok - first_new;
-    const uint16_t* src =
-        ch < DK / 8 ? p.new_k + (int64_t)(u.qo_begin + i) * p.nk_stride_tok +
-                          (int64_t)u.h_kv * p.nk_stride_head + 8 * ch
-                    : p.new_v + (int64_t)(u.qo_begin + i) * p.nv_stride_tok +
-                          (int64_t)u.h_kv * p.nv_stride_head + 8 * (ch - DK / 8);
-    cp_async_16(sNew + (tok - new_lo) * T::NEW_ROW + 16 * ch, src);
-  }
-  __syncthreads();  // barriers initialised, amax slots zeroed
+  qsync();  // amax slots zeroed
 
   // ---- the page pipeline: lane 0 copies, everyone waits on the stage -----
   uint8_t* wpipe = pipe + warp * STAGES * T::STAGE_BYTES;
@@ -250,16 +250,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
     uint8_t* st = wpipe + js * T::STAGE_BYTES;
     if (lane == 0) sPid[warp * STAGES + js] = pid;
     const uint32_t pg = (uint32_t)max(pid, 0);
-    if constexpr (BULK) {
-      if (lane == 0) {
-        uint64_t* bar = &wbar[j % STAGES];
-        mbar_expect_tx(bar, T::STAGE_BYTES);
-        bulk_g2s(st, kb + (uint64_t)pg * ksp, T::K_BYTES, bar);
-        bulk_g2s(st + T::OFF_V, vb + (uint64_t)pg * vsp, T::V_BYTES, bar);
-        bulk_g2s(st + T::OFF_KSF, ksb + (uint64_t)pg * kssp, T::KSF_BYTES, bar);
-        bulk_g2s(st + T::OFF_VSF, vsb + (uint64_t)pg * vssp, T::VSF_BYTES, bar);
-      }
-    } else {
+    {
       (void)st;
       const uint32_t so = js * T::STAGE_BYTES;
       const uint8_t* ks = kl + (uint64_t)pg * ksp;
@@ -278,9 +269,8 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
   for (int j = 0; j < STAGES - 1; ++j) {
     const int32_t pid = __shfl_sync(0xffffffffu, ids_cur, j);
     if (j < npw) issue(j, pid, j);
-    else if constexpr (!BULK) cp_async_commit();
+    else cp_async_commit();
   }
-
   // ---- Q: per-row power-of-two prescale into f16, row limits ------------
 #pragma unroll
   for (int k = 0; k < QPT; ++k) {
@@ -294,7 +284,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
                            fabsf(bf16_bits_to_f32(w[j] >> 16))));
     atomicMax(reinterpret_cast<int*>(sRowF) + ci / (DK / 8), __float_as_int(am));
   }
-  __syncthreads();
+  qsync();
 #pragma unroll
   for (int k = 0; k < QPT; ++k) {
     const int ci = tid + k * WARPS * 32;
@@ -320,32 +310,39 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
                                               __uint_as_float((uint32_t)(127 - e) << 23));
     }
   }
-  __syncthreads();
+  qsync();
 #pragma unroll
   for (int k = 0; k < QPT; ++k) {
     const int ci = tid + k * WARPS * 32;
     if (ci < QCH && ci % (DK / 8) == 0) sRowF[ci / (DK / 8)] = __uint_as_float(qv[k].x);
   }
-  __syncthreads();
+  qsync();
 
-  // this lane's query rows 2t and 2t+1: score factor f, -m_use, raise
-  // threshold (-inf until the row has a maximum, +inf for padding rows),
-  // causal limit, running max (log2) and partial sum
-  float f2[2], nm2[2], thr2[2], mrow[2], lrow[2], thr_lane;
-  int lim2[2];
+  // this lane's query rows 2t and 2t+1: score factor f, -m_use (the
+  // running max, log2 domain, once the row has one: bit k of has_max) and
+  // partial sum.  A row's raise threshold is 2^8 once it has a maximum, -inf
+  // before (any score raises), +inf for a padding row (never); thr_lane is
+  // the smaller of the lane's two.  The causal limits stay in sRowLim.
+  float f2[2], nm2[2], lrow[2];
+  uint32_t has_max = 0;
   int min_lim = INT32_MAX;
   for (int rr = 0; rr < T::RB; ++rr)
     if (sRowLim[rr] >= 0) min_lim = min(min_lim, sRowLim[rr]);
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     f2[k] = sRowF[2 * t + k];
-    lim2[k] = sRowLim[2 * t + k];
     nm2[k] = 0.f;
-    thr2[k] = lim2[k] >= 0 ? -INFINITY : INFINITY;
-    mrow[k] = -INFINITY;
     lrow[k] = 0.f;
   }
-  thr_lane = fminf(thr2[0], thr2[1]);
+  auto lane_threshold = [&]() {
+    float th = INFINITY;
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      th = fminf(th, (has_max >> k) & 1u ? kDecRaiseLog2
+                                         : (sRowLim[2 * t + k] >= 0 ? -INFINITY : INFINITY));
+    return th;
+  };
+  float thr_lane = lane_threshold();
   // Q fragments (the B operand of S^T): k-step kk covers the 4 dims at
   // 2 (4c + t) CB + 4m for chunk c = kk / KS_PER_CH, step m
   uint32_t qreg[T::KSTEPS][2];
@@ -362,13 +359,11 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
 #pragma unroll
     for (int k = 0; k < 4; ++k) oacc[mt][k] = 0.f;
 
-  // quantise the new tokens of page i (stage st) into the cache and the stage
-  auto patch_new = [&](int i, uint8_t* st, int tok0) {
+  auto patch_new = [&](uint8_t* st, int tok0, int is) {
     const int lo = max(new_lo, tok0), hi = min(new_hi, tok0 + 16);
     if (lo >= hi) return;
-    if constexpr (BULK) cp_async_wait<0>();  // the prefetch of the bf16 rows
     __syncwarp();
-    const int32_t pid = sPid[warp * STAGES + i % STAGES];
+    const int32_t pid = sPid[warp * STAGES + is];
     constexpr int NB = DK / 16 + DV / 16;
     const CacheView& cv = p.cache;
     for (int idx = lane; idx < (hi - lo) * NB; idx += 32) {
@@ -406,14 +401,15 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
   // the second row of each pair is an immediate 8 rows further on)
   static_assert(T::NCH == 1, "one K chunk per lane");
   const int kr0 = tok_of(g), vt0 = tok_of(2 * t), vt1 = vt0 ^ 1;
-  // byte offsets in a stage: K row kr0 at the lane's chunk t, its scale
-  // pair, V rows vt0 / vt1 at byte g VC, their scales at block g VC / 8
-  const uint32_t o_k = kr0 * T::KROW + t * T::CB;
-  const uint32_t o_ks = T::OFF_KSF + kr0 * T::KSFROW + t * (T::CB / 8);
-  const uint32_t o_v0 = T::OFF_V + vt0 * T::VROW + g * T::VC;
-  const uint32_t o_v1 = T::OFF_V + vt1 * T::VROW + g * T::VC;
-  const uint32_t o_vs0 = T::OFF_VSF + vt0 * T::VSFROW + (g * T::VC) / 8;
-  const uint32_t o_vs1 = T::OFF_VSF + vt1 * T::VSFROW + (g * T::VC) / 8;
+  // shared addresses in stage 0 (stage s is s * STAGE_BYTES further on): K
+  // row kr0 at the lane's chunk t, its scale pair, V rows vt0 / vt1 at byte
+  // g VC, their scales at block g VC / 8
+  const uint32_t o_k = wpipe_s + kr0 * T::KROW + t * T::CB;
+  const uint32_t o_ks = wpipe_s + T::OFF_KSF + kr0 * T::KSFROW + t * (T::CB / 8);
+  const uint32_t o_v0 = wpipe_s + T::OFF_V + vt0 * T::VROW + g * T::VC;
+  const uint32_t o_v1 = wpipe_s + T::OFF_V + vt1 * T::VROW + g * T::VC;
+  const uint32_t o_vs0 = wpipe_s + T::OFF_VSF + vt0 * T::VSFROW + (g * T::VC) / 8;
+  const uint32_t o_vs1 = wpipe_s + T::OFF_VSF + vt1 * T::VSFROW + (g * T::VC) / 8;
   // Pages whose tokens reach the smallest row limit need the causal /
   // length mask, and pages holding this step's new tokens need the patch:
   // both sit at the end of the unit, so the loop runs a lean body over the
@@ -426,11 +422,9 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
     const int unit_ok = ok >= 0 ? ok / 16 + 1 : 0;
     n_lean = unit_ok > warp ? min(npw, (unit_ok - warp + WARPS - 1) / WARPS) : 0;
   }
-  int fail_at = -1;
-  // one page; false when its copy wait ran out
   // page i, held in stage is (= i % STAGES: a constant where the caller
   // unrolls, so the stage offsets become immediates)
-  auto page = [&](int i, auto special, int is) -> bool {
+  auto page = [&](int i, auto special, int is) {
     constexpr bool SP = decltype(special)::value;
     const int j = i + STAGES - 1;
     if (j < npw) {
@@ -439,29 +433,17 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
         ids_nxt = load_ids(j / 32 + 1);
       }
       issue(j, __shfl_sync(0xffffffffu, ids_cur, j & 31), (is + STAGES - 1) % STAGES);
-    } else if constexpr (!BULK) {
+    } else {
       cp_async_commit();  // keep one group per page for the wait count
     }
-    if constexpr (BULK) {
-      bool landed = true;
-      if (lane == 0) landed = dec_wait(&wbar[i % STAGES], (i / STAGES) & 1);
-      landed = __shfl_sync(0xffffffffu, landed, 0);
-      __syncwarp();  // orders lane 0's observation of the copies before the reads
-      if (!landed) {
-        if (lane == 0) atomicOr(p.flags, 0x4u);
-        fail_at = i;
-        return false;
-      }
-    } else {
-      cp_async_wait<STAGES - 1>();
-      __syncwarp();
-    }
+    cp_async_wait<STAGES - 1>();
+    __syncwarp();
     const uint32_t so = is * T::STAGE_BYTES;
     const int tok0 = u.tok_begin + (warp + i * WARPS) * 16;
     if constexpr (SP) {
-      if (new_lo < new_hi) patch_new(i, wpipe + so, tok0);
+      if (new_lo < new_hi) patch_new(wpipe + so, tok0, is);
     }
-    const uint32_t sb = wpipe_s + so;
+    const uint32_t sb = so;
 
     // V rows vt0, vt1, vt0 + 8, vt1 + 8 and their scales
     constexpr int VW = T::VC / 4 > 0 ? T::VC / 4 : 1;
@@ -538,10 +520,11 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
     for (int k = 0; k < 4; ++k) x[k] = fmaf(sa[k] + sb4[k], f2[k & 1], nm2[k & 1]);
     if (SP && tok0 + 15 > min_lim) {
       const int ta = tok0 + kr0, tb = ta + 8;
-      if (ta > lim2[0]) x[0] = -INFINITY;
-      if (ta > lim2[1]) x[1] = -INFINITY;
-      if (tb > lim2[0]) x[2] = -INFINITY;
-      if (tb > lim2[1]) x[3] = -INFINITY;
+      const int l0 = sRowLim[2 * t], l1 = sRowLim[2 * t + 1];
+      if (ta > l0) x[0] = -INFINITY;
+      if (ta > l1) x[1] = -INFINITY;
+      if (tb > l0) x[2] = -INFINITY;
+      if (tb > l1) x[3] = -INFINITY;
     }
     // raise test against the lane's smaller threshold (a superset of the
     // rows that need it: the raise itself works per row)
@@ -558,17 +541,17 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
       float corr[2] = {1.f, 1.f};
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        if (mx[k] != -INFINITY && (mrow[k] == -INFINITY || mx[k] > 0.f)) {
-          if (mrow[k] != -INFINITY) corr[k] = ex2(-mx[k]);  // 2^(m_old - m_new)
-          mrow[k] = (mrow[k] == -INFINITY ? 0.f : mrow[k]) + mx[k];
-          nm2[k] = -mrow[k];
-          thr2[k] = kDecRaiseLog2;
-          thr_lane = fminf(thr2[0], thr2[1]);
+        const bool has = (has_max >> k) & 1u;
+        if (mx[k] != -INFINITY && (!has || mx[k] > 0.f)) {
+          if (has) corr[k] = ex2(-mx[k]);  // 2^(m_old - m_new)
+          nm2[k] -= mx[k];                 // m_new = m_old + mx (0 + mx for a first max)
+          has_max |= 1u << k;
           x[k] -= mx[k];
           x[k + 2] -= mx[k];
         }
         lrow[k] *= corr[k];
       }
+      thr_lane = lane_threshold();
       if (corr[0] != 1.f || corr[1] != 1.f) {
 #pragma unroll
         for (int mt = 0; mt < T::MT; ++mt) {
@@ -616,34 +599,38 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
       }
     }
     __syncwarp();  // every lane has read the stage before lane 0 refills it
-    return true;
   };
-  {
-    int i = 0;
-#if NVFP4KV_DEC_UNROLL
-    for (; fail_at < 0 && i + STAGES <= n_lean; i += STAGES) {
+  // Rounds of STAGES pages: every warp of the CTA takes part in the same
+  // number of rounds (the CTA's largest) and works in as many as it has
+  // pages for.  A round of lean pages is unrolled (the stage offsets are
+  // then immediates); a round that reaches the tail pages, or the end, runs
+  // the full body page by page.
+  const int my_rounds = (npw + STAGES - 1) / STAGES;
+  if (lane == 0) atomicMax(s_rounds, my_rounds);
+  __syncthreads();  // (CTA-wide 2 of 2)
+  const int rounds = *s_rounds;
+  for (int r = 0; r < rounds; ++r) {
+    const int i = r * STAGES;
+    if (i + STAGES <= n_lean) {
 #pragma unroll
-      for (int k = 0; k < STAGES; ++k)
-        if (fail_at < 0) page(i + k, std::false_type{}, k);
+      for (int k = 0; k < STAGES; ++k) page(i + k, std::false_type{}, k);
+    } else {
+#pragma unroll 1
+      for (int k = 0; k < STAGES && i + k < npw; ++k) page(i + k, std::true_type{}, k);
     }
-#endif
-    if (fail_at < 0)
-      for (; i < n_lean; ++i)
-        if (!page(i, std::false_type{}, i % STAGES)) break;
-    if (fail_at < 0)
-      for (; i < npw; ++i)
-        if (!page(i, std::true_type{}, i % STAGES)) break;
-  }
-  if constexpr (!BULK) cp_async_wait<0>();
-  if (fail_at >= 0) {
-    // wind-down after a wait ran out: the copies still in flight (pages
-    // fail_at .. fail_at + STAGES - 1) complete before the CTA may exit
-    // (bounded like every other wait)
-    if (lane == 0)
-      for (int i = fail_at; i < min(npw, fail_at + STAGES); ++i)
-        dec_wait(&wbar[i % STAGES], (i / STAGES) & 1);
+    // pacing: round r done; wait until every warp has done round r - 1
+    if (lane == 0) {
+      mbar_arrive_one(&s_pace[r & 1]);
+      if (r >= 1) {
+        bool done = false;
+        for (int k = 0; k < kPacePolls && !done; ++k)
+          done = mbar_wait_hint(&s_pace[(r - 1) & 1], ((r - 1) >> 1) & 1, kPaceHintNs);
+        if (!done) atomicOr(p.flags, 0x10u);
+      }
+    }
     __syncwarp();
   }
+  cp_async_wait<0>();
 
   // ---- combine the warps ------------------------------------------------
 #pragma unroll
@@ -651,14 +638,14 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) lrow[k] += __shfl_xor_sync(0xffffffffu, lrow[k], o);
   }
-  __syncthreads();  // every warp is done with its pipeline buffers
+  qsync();  // every warp is done with its pipeline buffers
   float* sO = reinterpret_cast<float*>(pipe);   // [WARPS][RB][DV]
   float* sM = sO + WARPS * T::RB * DV;          // [WARPS][RB]
   float* sL = sM + WARPS * T::RB;               // [WARPS][RB]
   if (g == 0) {
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      sM[warp * T::RB + 2 * t + k] = mrow[k];
+      sM[warp * T::RB + 2 * t + k] = (has_max >> k) & 1u ? -nm2[k] : -INFINITY;
       sL[warp * T::RB + 2 * t + k] = lrow[k];
     }
   }
@@ -670,18 +657,12 @@ __global__ void __launch_bounds__(WARPS * 32, 4) attend_dec_kernel(const AttendP
     *reinterpret_cast<float2*>(o0) = make_float2(oacc[mt][0], oacc[mt][2]);
     *reinterpret_cast<float2*>(o1) = make_float2(oacc[mt][1], oacc[mt][3]);
   }
-  __syncthreads();
+  qsync();
 
-  finish_unit<T::RB, DV, WARPS>(p, u, 0, R, sM, sL, sO, sRowF);
+  finish_unit<T::RB, DV, WARPS>(p, u, 0, R, sM, sL, sO, sRowF, tid, qsync);
 }
 
-// Copy mechanism of the decode kernel: 1 = bulk copies on mbarriers, 0 =
-// per-lane 16-byte cp.async.
-#ifndef NVFP4KV_DEC_BULK
-#define NVFP4KV_DEC_BULK 0
-#endif
-
-template <int DK, int DV>
+template <int DK, int DV, int QUADS>
 bool make_dec(AttendConfig* cfg) {
   constexpr int WARPS = 4, STAGES = 4;
   using T = DecTraits<DK, DV, WARPS, STAGES>;
@@ -689,21 +670,24 @@ bool make_dec(AttendConfig* cfg) {
   cfg->dk = DK;
   cfg->dv = DV;
   cfg->rows = T::RB;
-  cfg->warps = WARPS;
-  cfg->smem_bytes = T::SMEM;
-  cfg->func = reinterpret_cast<const void*>(
-      attend_dec_kernel<DK, DV, WARPS, STAGES, NVFP4KV_DEC_BULK != 0>);
+  cfg->warps = WARPS * QUADS;
+  cfg->units_per_cta = QUADS;
+  cfg->smem_bytes = QUADS * T::SMEM_Q + 32;
+  cfg->func = reinterpret_cast<const void*>(attend_dec_kernel<DK, DV, WARPS, STAGES, QUADS>);
   return true;
 }
 
 }  // namespace
 
 // The decode kernel for (dk, dv) when a CTA has at most 8 query rows and the
-// cache's (page, head) regions are contiguous; false when not built.
-bool attend_config_dec(int dk, int dv, int rows, AttendConfig* cfg) {
-  if (rows > 8) return false;
-  if (dk == 64 && dv == 64) return make_dec<64, 64>(cfg);
-  if (dk == 128 && dv == 128) return make_dec<128, 128>(cfg);
+// cache's (page, head) regions are contiguous, with `quads` units per CTA (4,
+// or 1 for a grid of at most one unit per SM, where nothing competes and the
+// smaller CTA starts sooner); false when not built.
+bool attend_config_dec(int dk, int dv, int rows, int quads, AttendConfig* cfg) {
+  if (rows > 8 || (quads != 1 && quads != 4)) return false;
+  if (dk == 64 && dv == 64) return quads == 4 ? make_dec<64, 64, 4>(cfg) : make_dec<64, 64, 1>(cfg);
+  if (dk == 128 && dv == 128)
+    return quads == 4 ? make_dec<128, 128, 4>(cfg) : make_dec<128, 128, 1>(cfg);
   return false;
 }
 

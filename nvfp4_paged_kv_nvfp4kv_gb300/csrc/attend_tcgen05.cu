@@ -411,11 +411,16 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
     uint8_t* wst = sRaw + (warp - 8) * T::WST;
     // stage layout per warp: K chunks [2][32][16], V chunks [2][32][16],
     // K scales [32][4], V scales [32][4]
-    auto issue = [&](int t) {
+    // page id of this thread's token in tile t (-1 past the unit), loaded one
+    // tile before its copies are issued
+    auto load_pid = [&](int t) -> int32_t {
+      const int pg = (t * kTileTok + j) / p.page_size;
+      return (t < ntiles && pg < u.num_pages) ? __ldg(p.kv_indices + u.page_begin + pg) : -1;
+    };
+    auto issue = [&](int t, int32_t pid) {
       const int rel = t * kTileTok + j;
       const int pg = rel / p.page_size, slot = rel % p.page_size;
       if (pg >= u.num_pages) return;
-      int32_t pid = p.kv_indices[u.page_begin + pg];
       if (pid < 0 || pid >= c.num_pages) {
         atomicOr(p.flags, 0x1u);
         pid = 0;
@@ -434,11 +439,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
     };
 #pragma unroll
     for (int t = 0; t < RS - 1; ++t) {
-      if (t < ntiles) issue(t);
+      if (t < ntiles) issue(t, load_pid(t));
       cp_async_commit();
     }
+    int32_t pid_next = load_pid(RS - 1);
     for (int i = 0; i < ntiles; ++i) {
-      if (i + RS - 1 < ntiles) issue(i + RS - 1);
+      const int32_t pid = pid_next;
+      pid_next = load_pid(i + RS);
+      if (i + RS - 1 < ntiles) issue(i + RS - 1, pid);
       cp_async_commit();
       cp_async_wait<RS - 1>();  // this thread's copies of tile i landed
       const int bi = i % kKB;

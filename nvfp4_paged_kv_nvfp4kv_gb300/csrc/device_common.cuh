@@ -220,21 +220,25 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
 // request's current length: its planned whole pages plus the current length
 // of the last page (a value outside [1, page_size], or a length below the
 // request's query rows, sets flag 0x8 and is clamped).
-__device__ __forceinline__ WorkUnit load_unit(const AttendParams& p) {
-  WorkUnit u = p.units[blockIdx.x];
+__device__ __forceinline__ WorkUnit load_unit(const AttendParams& p, int idx, bool report) {
+  WorkUnit u = p.units[idx];
   if (p.live_last_page_len != nullptr) {
     const int P = p.page_size;
     const int full = (u.kv_len - 1) - (u.kv_len - 1) % P;  // tokens in whole pages
     int lpl = __ldg(p.live_last_page_len + u.b);
     int len = full + lpl;
     if (lpl < 1 || lpl > P || len < u.qo_len) {
-      if (threadIdx.x == 0) atomicOr(p.flags, 0x8u);
+      if (report) atomicOr(p.flags, 0x8u);
       lpl = max(1, min(P, lpl));
       len = max(u.qo_len, full + lpl);
     }
     u.kv_len = len;
   }
   return u;
+}
+// The unit of this CTA (one unit per CTA)
+__device__ __forceinline__ WorkUnit load_unit(const AttendParams& p) {
+  return load_unit(p, blockIdx.x, threadIdx.x == 0);
 }
 
 // Two f32 values as two packed output elements (bf16 or f16, lo from a).

@@ -27,8 +27,9 @@ cudaError_t prepare_kernel(const AttendConfig& cfg) {
 cudaError_t launch_attend(const AttendConfig& cfg, const AttendParams& p, int grid_x,
                           int grid_y, cudaStream_t stream) {
   void* args[] = {const_cast<AttendParams*>(&p)};
-  return cudaLaunchKernel(cfg.func, dim3(grid_x, grid_y), dim3(cfg.warps * 32), args,
-                          cfg.smem_bytes, stream);
+  const int upc = cfg.units_per_cta > 1 ? cfg.units_per_cta : 1;
+  return cudaLaunchKernel(cfg.func, dim3((grid_x + upc - 1) / upc, grid_y),
+                          dim3(cfg.warps * 32), args, cfg.smem_bytes, stream);
 }
 
 }  // namespace nvfp4kv

@@ -92,15 +92,15 @@ __device__ __forceinline__ void merge_if_last(const AttendParams& p, const WorkU
 
 // sM/sL: [WARPS][RB] running max (log2 domain) and sum of each warp;
 // sO: [WARPS][RB][DV] each warp's un-normalised output rows;
-// sFin: scratch of at least 2*RB floats + 1 int.
-template <int RB, int DV, int WARPS>
+// sFin: scratch of at least 2*RB floats + 1 int.  Run by the unit's
+// WARPS * 32 threads (tid in [0, WARPS * 32)), which synchronise with `sync`.
+template <int RB, int DV, int WARPS, class Sync>
 __device__ __forceinline__ void finish_unit(const AttendParams& p, const WorkUnit& u,
                                             int row0, int R, const float* sM,
                                             const float* sL, const float* sO,
-                                            float* sFin) {
+                                            float* sFin, int tid, Sync sync) {
   using namespace dev;
   constexpr float kLn2 = 0.69314718055994530942f;
-  const int tid = threadIdx.x;
   const int G = p.group, Hq = p.num_qo_heads;
   const bool partial = p.split && u.num_splits > 1;
 
@@ -142,7 +142,17 @@ __device__ __forceinline__ void finish_unit(const AttendParams& p, const WorkUni
   }
   if (!partial) return;
 
-  merge_if_last<RB, DV, WARPS * 32, 20>(p, u, row0, R, sFin, tid, [] { __syncthreads(); });
+  merge_if_last<RB, DV, WARPS * 32, 20>(p, u, row0, R, sFin, tid, sync);
+}
+
+// The same for a CTA that is one unit (all its threads, __syncthreads).
+template <int RB, int DV, int WARPS>
+__device__ __forceinline__ void finish_unit(const AttendParams& p, const WorkUnit& u,
+                                            int row0, int R, const float* sM,
+                                            const float* sL, const float* sO,
+                                            float* sFin) {
+  finish_unit<RB, DV, WARPS>(p, u, row0, R, sM, sL, sO, sFin, (int)threadIdx.x,
+                             [] { __syncthreads(); });
 }
 
 }  // namespace nvfp4kv

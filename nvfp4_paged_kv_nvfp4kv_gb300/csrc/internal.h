@@ -54,6 +54,7 @@ struct AttendParams {
   CacheView cache;
   const int32_t* kv_indices;
   const WorkUnit* units;
+  int32_t num_units;    // work units of the launch
   int32_t num_qo_heads, group, causal, split;
   int32_t page_size;    // 16 or 1
   int32_t out_f16;      // output element: 0 bf16, 1 f16
@@ -123,6 +124,7 @@ struct AttendConfig {
   int rows;       // query rows per CTA (8 or 16; 16, 32 or 64 for tcgen05)
   int warps;
   int smem_bytes;
+  int units_per_cta;  // work units one CTA runs (0 or 1: one)
   const void* func;  // kernel entry (for occupancy queries)
 };
 

@@ -5,11 +5,13 @@
 // e2m1_RNE_satfinite(x_i / (s g)), ties to the even code, zero codes keep the
 // sign of x_i, low nibble = even element.  Every rounding decision is the
 // exact-real one, in float32 only:
-//  * an approximate t = amax / g / 6 (two correctly rounded divisions, a few
-//    ulps from the exact ratio) is rounded to E4M3 by the hardware RN
-//    conversion; the E4M3 grid is 2^-4 relative or coarser, so the exact
-//    answer is that code or a neighbour, decided by comparing amax with
-//    6 * midpoint * g exactly;
+//  * an approximate t = amax * RN(1 / RN(6 g)) (a few ulps from the exact
+//    ratio; the reciprocal does not depend on the data) is rounded to E4M3 by
+//    the hardware RN conversion; the E4M3 grid is 2^-4 relative or coarser,
+//    so the exact answer is that code or a neighbour, decided by comparing
+//    amax with 6 * midpoint * g exactly (t overflows to inf only far above
+//    the saturation point and underflows to 0 only far below the first
+//    midpoint);
 //  * element codes compare |x| with the seven e2m1 midpoints times s g.
 // An exact comparison of a with m * g (m, g, a positive floats): m * g = P + E
 // exactly with P = RN(m g) and E = fma(m, g, -P); a - P is exact when a and P
@@ -40,9 +42,10 @@ __device__ __forceinline__ int cmp_prod(float a, float m, float g) {
 }
 
 // E4M3 code of amax / (6 g): round to nearest even, saturating at 448.
-__device__ __forceinline__ uint32_t scale_code(float amax, float g) {
+// inv6g: RN(1 / RN(6 g)).
+__device__ __forceinline__ uint32_t scale_code(float amax, float g, float inv6g) {
   if (amax == 0.f) return 0u;
-  const float t = __fdiv_rn(__fdiv_rn(amax, g), 6.0f);
+  const float t = __fmul_rn(amax, inv6g);
   unsigned short pair;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(pair) : "f"(0.0f), "f"(t));
   uint32_t c = pair & 0xFFu;
@@ -71,10 +74,11 @@ __device__ __forceinline__ uint32_t quantize_block16(uint4 lo, uint4 hi, float g
     x[2 * k] = __uint_as_float(wv[k] << 16);
     x[2 * k + 1] = __uint_as_float(wv[k] & 0xFFFF0000u);
   }
+  const float inv6g = __frcp_rn(__fmul_rn(6.0f, g));
   float amax = 0.f;
 #pragma unroll
   for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(x[k]));
-  const uint32_t sfb = scale_code(amax, g);
+  const uint32_t sfb = scale_code(amax, g, inv6g);
   const float s = e4m3_code_value(sfb);
   // thresholds T_k = mid_k * s * g: Tf_k = T_k rounded down to float32 and
   // whether that was exact.  |x| > T_k <=> |x| > Tf_k for a float |x|; a
