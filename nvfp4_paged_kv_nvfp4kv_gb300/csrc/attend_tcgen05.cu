@@ -13,7 +13,8 @@
 // query rows (N = 16, 32 or 64; the G heads of the group times the query
 // positions, padded).  Tiles of 128 tokens (8 pages) pass through three
 // roles; warp w works on tensor-memory lanes 32 (w % 4) .. + 31:
-//  * dequant (warps 8-15; thread = token, one half of the head dims): each
+//  * dequant (warps 8-11; thread = token, both halves of the head dims; 13
+//    warps in all, so every thread may hold 128 registers): each
 //    thread copies its own token's packed bytes and scale bytes RS - 1 tiles
 //    ahead (cp.async groups, no cross-thread hand-off), then e2m1 -> f16
 //    (cvt.rn.f16x2.e2m1x2) times the E4M3 block scale (exact in f16).  K_hat
@@ -23,7 +24,7 @@
 //  * softmax (warps 0-7; thread = token for S^T, = value dim for O^T, one
 //    half of the query-row columns): tcgen05.ld of its S^T row, p = 2^(x - m)
 //    written as the f16 P^T operand.
-//  * product issue (warp 16, one thread): S^T = K_hat . Q^T (M = 128 tokens,
+//  * product issue (warp 12, one thread): S^T = K_hat . Q^T (M = 128 tokens,
 //    N rows, K = Dk; A from tensor memory, B = Q in shared memory) into one
 //    of two tensor-memory tiles, and O^T += V_hat^T . P^T (M = 128 value
 //    dims, N rows, K = 128 tokens; both operands MN-major in shared memory)
@@ -54,7 +55,7 @@ namespace {
 using namespace dev;
 
 constexpr int kTileTok = 128;
-constexpr int kThreads = 544;  // softmax warps 0-7, dequant warps 8-15, issue warp 16
+constexpr int kThreads = 416;  // softmax warps 0-7, dequant warps 8-11, issue warp 12
 constexpr int kKB = 3;         // K_hat / V_hat buffers
 constexpr float kRaise = 8.f;  // log2 of the largest p before m is raised
 // Wait bounds (the defaults give up after about a second; a test build
@@ -373,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
 
   if (tid == 0) {
     for (int b = 0; b < kKB; ++b) {
-      mbar_init(&kv_full[b], 8);
+      mbar_init(&kv_full[b], 4);
       mbar_init(&kv_empty[b], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -403,14 +404,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  if (warp >= 8 && warp < 16) {
-    // ================= dequant (thread = token, half the dims) ===========
+  if (warp >= 8 && warp < 12) {
+    // ================= dequant (thread = token, all head dims) ===========
     const CacheView& c = p.cache;
-    const int hd = (warp - 8) >> 2;  // dims [64 hd, 64 hd + 64)
     // this thread's token j of tile t: page rel / page_size, slot rel % page_size
-    uint8_t* wst = sRaw + (warp - 8) * T::WST;
-    // stage layout per warp: K chunks [2][32][16], V chunks [2][32][16],
-    // K scales [32][4], V scales [32][4]
+    // stage layout per (warp, half hd of the dims): K chunks [2][32][16], V
+    // chunks [2][32][16], K scales [32][4], V scales [32][4]
+    auto wst = [&](int hd) { return sRaw + (4 * hd + q4) * T::WST; };
     // page id of this thread's token in tile t (-1 past the unit), loaded one
     // tile before its copies are issued
     auto load_pid = [&](int t) -> int32_t {
@@ -425,17 +425,20 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
         atomicOr(p.flags, 0x1u);
         pid = 0;
       }
-      uint8_t* st = wst + (t % RS) * T::STAGE;
-      const uint8_t* kr = c.k_data + pid * c.k_sp + u.h_kv * c.k_sh + slot * c.k_ss + 32 * hd;
-      const uint8_t* vr = c.v_data + pid * c.v_sp + u.h_kv * c.v_sh + slot * c.v_ss + 32 * hd;
-      cp_async_16(st + lane * 16, kr);
-      cp_async_16(st + 512 + lane * 16, kr + 16);
-      cp_async_16(st + 1024 + lane * 16, vr);
-      cp_async_16(st + 1536 + lane * 16, vr + 16);
-      cp_async_small<4>(st + 2048 + lane * 4,
-                        c.k_sf + pid * c.ksf_sp + u.h_kv * c.ksf_sh + slot * c.ksf_ss + 4 * hd);
-      cp_async_small<4>(st + 2176 + lane * 4,
-                        c.v_sf + pid * c.vsf_sp + u.h_kv * c.vsf_sh + slot * c.vsf_ss + 4 * hd);
+      const uint8_t* kr = c.k_data + pid * c.k_sp + u.h_kv * c.k_sh + slot * c.k_ss;
+      const uint8_t* vr = c.v_data + pid * c.v_sp + u.h_kv * c.v_sh + slot * c.v_ss;
+      const uint8_t* ks = c.k_sf + pid * c.ksf_sp + u.h_kv * c.ksf_sh + slot * c.ksf_ss;
+      const uint8_t* vs = c.v_sf + pid * c.vsf_sp + u.h_kv * c.vsf_sh + slot * c.vsf_ss;
+#pragma unroll
+      for (int hd = 0; hd < 2; ++hd) {
+        uint8_t* st = wst(hd) + (t % RS) * T::STAGE;
+        cp_async_16(st + lane * 16, kr + 32 * hd);
+        cp_async_16(st + 512 + lane * 16, kr + 32 * hd + 16);
+        cp_async_16(st + 1024 + lane * 16, vr + 32 * hd);
+        cp_async_16(st + 1536 + lane * 16, vr + 32 * hd + 16);
+        cp_async_small<4>(st + 2048 + lane * 4, ks + 4 * hd);
+        cp_async_small<4>(st + 2176 + lane * 4, vs + 4 * hd);
+      }
     };
 #pragma unroll
     for (int t = 0; t < RS - 1; ++t) {
@@ -458,7 +461,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
       }
       tc_fence_after();
       const bool valid = u.tok_begin + i * kTileTok + j < tok_end;
-      const uint8_t* st = wst + (i % RS) * T::STAGE;
+#pragma unroll
+      for (int hd = 0; hd < 2; ++hd) {
+      const uint8_t* st = wst(hd) + (i % RS) * T::STAGE;
       // ---- K_hat: tensor memory columns 64 bi + 32 hd + [0, 32) -----------
       {
         const uint32_t sf = *reinterpret_cast<const uint32_t*>(st + 2048 + lane * 4);
@@ -501,6 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
           }
         }
       }
+      }  // hd
       tmem_wait_st();
       fence_async_smem();
       tc_fence_before();
@@ -510,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
       if (lane == 0 && !withhold) mbar_arrive(&kv_full[bi]);
     }
     cp_async_wait<0>();
-  } else if (warp == 16) {
+  } else if (warp == 12) {
     // ================= product issue (one thread) =========================
     if (lane == 0) {
       // descriptors of the first k-step; later k-steps advance the start
