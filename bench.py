@@ -424,6 +424,85 @@ def run_gpu(args, world, rank, local):
 # CPU oracle (baseline and reference arm)
 # ---------------------------------------------------------------------------
 
+def run_op(args, local):
+    """The library's standalone operations on the workload's sizes (not the
+    benchmark's metric: one JSON line per op for their profiles).
+
+    merge_states: the float32 partial states of the workload's split plan
+    (random values; every (query row, head) merges the plan's number of
+    splits) folded into bf16 out + lse.  dequantize: every page of the
+    workload's cache (quantised from its K/V) to float32 K and V.  GB/s counts
+    the bytes each op must read and write."""
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = W.WORKLOADS[args.workload]
+    batch = W.make_batch(cfg)
+    c = cfg
+    g = torch.Generator().manual_seed(cfg.seed + 101)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(512 << 20, dtype=torch.uint8, device=dev)
+    if args.op == "merge_states":
+        plan = N.nvfp4kv_decode_plan(batch.qo_indptr, batch.kv_indptr, batch.last_page_len,
+                                     c.num_qo_heads, c.num_kv_heads, c.head_dim_qk,
+                                     c.head_dim_vo, causal=c.causal, device=local,
+                                     allocate=False)
+        splits = max(1, int(plan.info.max_units_per_request))
+        E = int(batch.qo_indptr[-1]) * c.num_qo_heads
+        P = E * splits
+        po = torch.randn((P, c.head_dim_vo), generator=g).to(dev)
+        pl = (torch.randn((P,), generator=g) * 4).to(dev)
+        mi = (torch.arange(E + 1, dtype=torch.int32) * splits).to(dev)
+        run = lambda: N.nvfp4kv_merge_states(po, pl, mi)
+        nbytes = P * (c.head_dim_vo + 1) * 4 + (E + 1) * 4 + E * (c.head_dim_vo * 2 + 4)
+        desc = "%d (row, head) entries x %d partial states, Dv=%d" % (E, splits, c.head_dim_vo)
+    else:
+        lay = batch.cache_layout(args.layout)
+        cache = N.PagedCache.allocate(lay, batch.k_global_scale, batch.v_global_scale,
+                                      device=dev)
+        i32 = lambda t: torch.as_tensor(t).to(torch.int32).to(dev)
+        kv_indices, kv_indptr, last = i32(batch.kv_indices), i32(batch.kv_indptr), \
+            i32(batch.last_page_len)
+        for ts in (batch.prefix, batch.new):
+            for s0 in range(0, ts.k.shape[0], 1 << 16):
+                N.nvfp4kv_quantize_append(cache, ts.k[s0:s0 + (1 << 16)].to(dev),
+                                          ts.v[s0:s0 + (1 << 16)].to(dev),
+                                          i32(ts.batch_idx[s0:s0 + (1 << 16)]),
+                                          i32(ts.positions[s0:s0 + (1 << 16)]),
+                                          kv_indices, kv_indptr, last)
+        pages = kv_indices
+        n = int(pages.numel())
+        k_out = torch.empty((n, 16, c.num_kv_heads, c.head_dim_qk), dtype=torch.float32,
+                            device=dev)
+        v_out = torch.empty((n, 16, c.num_kv_heads, c.head_dim_vo), dtype=torch.float32,
+                            device=dev)
+        run = lambda: N.nvfp4kv_dequantize_paged(cache, pages, k_out=k_out, v_out=v_out)
+        elts = n * 16 * c.num_kv_heads
+        nbytes = (elts * (c.head_dim_qk + c.head_dim_vo) * (0.5 + 1 / 16 + 4) + n * 4)
+        desc = "%d pages x 16 tokens x %d kv heads, Dqk=%d Dvo=%d" % (
+            n, c.num_kv_heads, c.head_dim_qk, c.head_dim_vo)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    t = []
+    for _ in range(args.steps):
+        if args.l2_flush != "none":
+            flush.fill_(1)
+            flush_r.max()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        run()
+        b.record(stream)
+        t.append((a, b))
+    torch.cuda.synchronize()
+    ms = statistics.mean(x.elapsed_time(y) for x, y in t)
+    return {"op": args.op, "metric": "standalone %s: achieved GB/s" % args.op,
+            "value": nbytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "steps": args.steps, "warmup": args.warmup, "bytes_per_step": nbytes,
+            "config": {"workload": workload_desc(cfg), "op": desc,
+                       "l2": "flushed between steps" if args.l2_flush != "none" else "not flushed"}}
+
+
 def _oracle():
     sys.path.insert(0, os.path.join(ROOT, "oracle"))
     import oracle as O
@@ -591,13 +670,18 @@ def main():
                     help="skip the end-to-end leg (profiler captures)")
     ap.add_argument("--separate-append", action="store_true",
                     help="quantize_append and decode_run as two launches per step")
+    ap.add_argument("--op", default="attention", choices=["attention", "merge_states", "dequantize"],
+                    help="time one of the library's standalone operations on the workload's "
+                         "sizes instead (for their profiles; not the benchmark's metric)")
     args = ap.parse_args()
     if args.kernel == 2:  # the CUDA-core comparison kernel has no fused append
         args.separate_append = True
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world, rank, local = init_dist()
-    if args.impl == "reference":
+    if args.op != "attention":
+        res = run_op(args, local) if rank == 0 else None
+    elif args.impl == "reference":
         res = run_reference(args, world, rank)
     else:
         res = run_gpu(args, world, rank, local)
