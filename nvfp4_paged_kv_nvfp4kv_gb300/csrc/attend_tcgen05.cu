@@ -833,6 +833,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
       const bool partial = p.split && u.num_splits > 1;
       const int Hq = p.num_qo_heads;
       if (active) {
+        // The row sum, the normaliser and the output row of a column are the
+        // same in every lane: lane e (mod CW) derives them for column e of the
+        // chunk, once, and the warp reads them back by shuffle.
+        const int e_l = lane & (CW - 1);
+        uint16_t* const out_u = p.out + (int64_t)u.qo_begin * Hq * DV;
+        float* const part_u = partial ? p.partial_o + (int64_t)u.partial_base * DV : nullptr;
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
           uint32_t ov[CW], lv[CW];
@@ -840,26 +846,37 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
           tmem_ld<CW>(tmem + lane_base + T::LCOL + c0 + ch * CW, lv);
           tmem_wait_ld<CW>(ov);
           tmem_wait_ld<CW>(lv);
+          float L = __uint_as_float(lv[0]);
+#pragma unroll
+          for (int e = 1; e < CW; ++e) L = e_l == e ? __uint_as_float(lv[e]) : L;
+          const int col_l = c0 + ch * CW + e_l;
+          float f_l = 0.f;
+          int off_l = 0;  // output row of the column, from the unit's first row
+          if (col_l < nvalid) {
+            const float m = s_m[col_l];
+            const bool any = L > 0.f && m != -INFINITY;
+            f_l = any ? p.v_scale / L : 0.f;
+            const float lse_v = any ? (m + log2f(L)) * kLn2 : -INFINITY;
+            const int gr = row0 + col_l, qi = gr / G, head = u.h_kv * G + gr % G;
+            off_l = partial ? (qi * Hq + head) * u.num_splits + u.split : qi * Hq + head;
+            if (q4 == 0 && lane < CW) {
+              if (!partial) {
+                if (p.lse) p.lse[(int64_t)u.qo_begin * Hq + off_l] = lse_v;
+              } else {
+                p.partial_lse[(int64_t)u.partial_base + off_l] = lse_v;
+              }
+            }
+          }
 #pragma unroll
           for (int e = 0; e < CW; ++e) {
-            const int col = c0 + ch * CW + e, gr = row0 + col;
-            if (col < nvalid) {
-              const float L = __uint_as_float(lv[e]);
-              const float m = s_m[col];
-              const bool any = L > 0.f && m != -INFINITY;
-              const float o = any ? __uint_as_float(ov[e]) * (p.v_scale / L) : 0.f;
-              const float lse_v = any ? (m + log2f(L)) * kLn2 : -INFINITY;
-              const int qi = gr / G, head = u.h_kv * G + gr % G;
-              const int64_t qrow = u.qo_begin + qi;
-              if (!partial) {
-                p.out[(qrow * Hq + head) * DV + j] = pack_out1(o, p.out_f16);
-                if (j == 0 && p.lse) p.lse[qrow * Hq + head] = lse_v;
-              } else {
-                const int64_t pi = (int64_t)u.partial_base +
-                                   ((int64_t)qi * Hq + head) * u.num_splits + u.split;
-                p.partial_o[pi * DV + j] = o;
-                if (j == 0) p.partial_lse[pi] = lse_v;
-              }
+            const float f = __shfl_sync(0xffffffffu, f_l, e);
+            const int off = __shfl_sync(0xffffffffu, off_l, e);
+            if (c0 + ch * CW + e < nvalid) {
+              const float o = f != 0.f ? __uint_as_float(ov[e]) * f : 0.f;
+              if (!partial)
+                out_u[(int64_t)off * DV + j] = pack_out1(o, p.out_f16);
+              else
+                part_u[(int64_t)off * DV + j] = o;
             }
           }
         }
