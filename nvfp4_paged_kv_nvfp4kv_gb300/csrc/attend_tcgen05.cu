@@ -747,12 +747,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tcgen05_kernel(const Atten
         // ---- raise this half's running maxima to the tile's row maxima ----
         if (gtid < NH) s_max[c0 + gtid] = INT32_MIN;
         named_sync(gbar, 128);
-        if (active) {
+        if (active) {  // lane e keeps column e's warp maximum: one atomic per lane
+          int kk = INT32_MIN;
 #pragma unroll
           for (int e = 0; e < NH; ++e) {
             const int k = __reduce_max_sync(0xffffffffu, fkey(tok_ok ? x[e] : -INFINITY));
-            if (lane == 0) atomicMax(&s_max[c0 + e], k);
+            kk = lane == e ? k : kk;
           }
+          if (lane < NH) atomicMax(&s_max[c0 + lane], kk);
         }
         named_sync(gbar, 128);
         bool moved = false;
