@@ -36,11 +36,17 @@ from nvfp4_paged_kv_nvfp4kv_gb300 import workloads as W  # noqa: E402
 METRIC = "NVFP4 paged decode: µs/call, KV tokens/s, achieved HBM GB/s vs GB300 peak"
 UNIT = "KV tokens/s"
 FALLBACK_HBM_GBS = 6800.0
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attend_dec_long_context_decode.json")
-KERNEL_SOURCES = [os.path.join(ROOT, "nvfp4_paged_kv_nvfp4kv_gb300", "csrc", f)
-                  for f in ("attend_dec.cu", "attend_tc.cu", "append_fused.cuh",
-                            "device_common.cuh", "epilogue.cuh", "internal.h", "quantize.cuh",
-                            "stage.cuh")]
+_CSRC = os.path.join(ROOT, "nvfp4_paged_kv_nvfp4kv_gb300", "csrc")
+_COMMON = ("append_fused.cuh", "device_common.cuh", "epilogue.cuh", "internal.h", "quantize.cuh")
+# per workload: the committed ncu summary of its dominant kernel and the
+# sources that kernel is built from (the DRAM bytes are used only while the
+# sources still hash to the value the summary was taken on)
+TRAFFIC = {
+    "long_context_decode": ("attend_dec_long_context_decode.json",
+                            ("attend_dec.cu", "attend_tc.cu") + _COMMON + ("stage.cuh",)),
+    "prefix_cache_extend": ("attend_tcgen05_prefix_cache_extend.json",
+                            ("attend_tcgen05.cu",) + _COMMON),
+}
 
 
 def workload_desc(cfg: W.Workload) -> str:
@@ -77,23 +83,27 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_hash() -> str:
+def kernel_hash(sources) -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
-        with open(p, "rb") as f:
+    for name in sources:
+        with open(os.path.join(_CSRC, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def traffic_per_launch(n_units_kv_bytes: int):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
+def traffic_per_launch(workload: str):
+    """DRAM bytes per launch of the workload's dominant kernel from its
+    committed ncu summary, if one exists for this workload and was taken on
+    the current kernel source (else None)."""
+    if workload not in TRAFFIC:
+        return None
+    fname, sources = TRAFFIC[workload]
     try:
-        with open(TRAFFIC_FILE) as f:
+        with open(os.path.join(ROOT, "profiles", fname)) as f:
             d = json.load(f)
     except Exception:
         return None
-    if d.get("kernel_hash") != kernel_hash():
+    if d.get("workload") != workload or d.get("kernel_hash") != kernel_hash(sources):
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -378,7 +388,7 @@ def run_gpu(args, world, rank, local):
     alg = algorithmic_bytes(batch, fused_append=not args.separate_append)
     ms_attend = statistics.mean(t_attend)
     achieved = alg / (ms_attend * 1e-3) / 1e9
-    traffic = traffic_per_launch(alg)
+    traffic = traffic_per_launch(cfg.name)
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step_max,
