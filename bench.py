@@ -43,7 +43,8 @@ _COMMON = ("append_fused.cuh", "device_common.cuh", "epilogue.cuh", "internal.h"
 # sources still hash to the value the summary was taken on)
 TRAFFIC = {
     "long_context_decode": ("attend_dec_long_context_decode.json",
-                            ("attend_dec.cu", "attend_tc.cu") + _COMMON + ("stage.cuh",)),
+                            ("attend_dec.cu", "device_common.cuh", "epilogue.cuh", "internal.h",
+                             "quantize.cuh")),
     "prefix_cache_extend": ("attend_tcgen05_prefix_cache_extend.json",
                             ("attend_tcgen05.cu",) + _COMMON),
 }
