@@ -404,3 +404,133 @@ done:
   free(lc);
   return rc;
 }
+
+/* ---- attention with FP4 query and probabilities ------------------------ */
+
+/* x -> NVFP4 (orc_quantize_block16 with global scale 1) -> value. */
+static void fp4_round16(const double x[16], double y[16]) {
+  uint8_t packed[8], sf;
+  double s;
+  int i;
+  orc_quantize_block16(x, 1.0, packed, &sf);
+  s = orc_e4m3_value(sf);
+  for (i = 0; i < 16; ++i)
+    y[i] = orc_e2m1_value((uint8_t)((packed[i / 2] >> (4 * (i & 1))) & 15)) * s;
+}
+
+int orc_attention_unit_fp4qp(const orc_cache* c, const orc_page_table* pt,
+                             const int32_t* qo_indptr, const uint16_t* q_bf16,
+                             int64_t q_stride_tok, int64_t q_stride_head,
+                             int32_t num_qo_heads, int32_t causal,
+                             double sm_scale, int32_t b, int32_t h_kv,
+                             double* out, double* lse) {
+  const double kPScale = 448.0 * 6.0;
+  int32_t G, nq, rows, r, i, g, d, page, slot, t;
+  int32_t dk = c->head_dim_qk, dv = c->head_dim_vo;
+  int64_t L, q0, j, blk;
+  double *qv = NULL, *s = NULL, *M = NULL, *Z = NULL, *o = NULL, *kr = NULL,
+         *vb = NULL;
+  int64_t* limit = NULL;
+  int rc = ORC_OK;
+  if (num_qo_heads <= 0 || c->num_kv_heads <= 0 ||
+      num_qo_heads % c->num_kv_heads || b < 0 || b >= pt->batch || h_kv < 0 ||
+      h_kv >= c->num_kv_heads || dk % 16)
+    return ORC_BAD_ARGUMENT;
+  G = num_qo_heads / c->num_kv_heads;
+  q0 = qo_indptr[b];
+  nq = qo_indptr[b + 1] - qo_indptr[b];
+  L = orc_kv_len(pt, b, c->page_size);
+  if (nq > L) return ORC_BAD_ARGUMENT;
+  rows = nq * G;
+  if (rows == 0) return ORC_OK;
+  qv = (double*)malloc(sizeof(double) * rows * dk);
+  s = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * rows);
+  M = (double*)malloc(sizeof(double) * rows);
+  Z = (double*)malloc(sizeof(double) * rows);
+  o = (double*)malloc(sizeof(double) * rows * dv);
+  kr = (double*)malloc(sizeof(double) * dk);
+  vb = (double*)malloc(sizeof(double) * 16 * dv);
+  limit = (int64_t*)malloc(sizeof(int64_t) * rows);
+  if (!qv || !s || !M || !Z || !o || !kr || !vb || !limit) {
+    rc = ORC_BAD_ARGUMENT;
+    goto done;
+  }
+  /* row r = i * G + g: the query row quantised per 16 dims */
+  for (i = 0; i < nq; ++i)
+    for (g = 0; g < G; ++g) {
+      double x[16];
+      r = i * G + g;
+      for (d = 0; d < dk; d += 16) {
+        for (t = 0; t < 16; ++t)
+          x[t] = orc_bf16_value(q_bf16[(q0 + i) * q_stride_tok +
+                                       (h_kv * G + g) * q_stride_head + d + t]);
+        fp4_round16(x, qv + (int64_t)r * dk + d);
+      }
+      limit[r] = causal ? (L - nq + i) : (L - 1);
+    }
+  /* scores with the quantised query, the row maxima and sums of exp */
+  for (j = 0; j < L; ++j) {
+    if (locate(c, pt, b, j, &page, &slot) != ORC_OK) {
+      rc = ORC_BAD_INDEX;
+      goto done;
+    }
+    orc_dequant_row(c, 0, page, slot, h_kv, kr);
+    for (r = 0; r < rows; ++r) {
+      double acc = 0.0;
+      for (d = 0; d < dk; ++d) acc += qv[(int64_t)r * dk + d] * kr[d];
+      s[j * rows + r] = sm_scale * acc;
+    }
+  }
+  for (r = 0; r < rows; ++r) {
+    M[r] = -INFINITY;
+    Z[r] = 0.0;
+    for (j = 0; j <= limit[r]; ++j) M[r] = fmax(M[r], s[j * rows + r]);
+    if (M[r] != -INFINITY)
+      for (j = 0; j <= limit[r]; ++j) Z[r] += exp(s[j * rows + r] - M[r]);
+    for (d = 0; d < dv; ++d) o[(int64_t)r * dv + d] = 0.0;
+  }
+  /* per block of 16 key positions: P' = 448 * 6 * p quantised, o += P_hat v */
+  for (blk = 0; blk * 16 < L; ++blk) {
+    for (t = 0; t < 16; ++t) {
+      j = blk * 16 + t;
+      if (j < L) {
+        locate(c, pt, b, j, &page, &slot);
+        orc_dequant_row(c, 1, page, slot, h_kv, vb + (int64_t)t * dv);
+      } else {
+        for (d = 0; d < dv; ++d) vb[(int64_t)t * dv + d] = 0.0;
+      }
+    }
+    for (r = 0; r < rows; ++r) {
+      double pp[16], ph[16];
+      if (M[r] == -INFINITY) continue;
+      for (t = 0; t < 16; ++t) {
+        j = blk * 16 + t;
+        pp[t] = (j < L && j <= limit[r]) ? kPScale * exp(s[j * rows + r] - M[r]) : 0.0;
+      }
+      fp4_round16(pp, ph);
+      for (t = 0; t < 16; ++t)
+        if (ph[t] != 0.0)
+          for (d = 0; d < dv; ++d)
+            o[(int64_t)r * dv + d] += ph[t] * vb[(int64_t)t * dv + d];
+    }
+  }
+  for (i = 0; i < nq; ++i)
+    for (g = 0; g < G; ++g) {
+      int64_t row = q0 + i, head = h_kv * G + g;
+      r = i * G + g;
+      for (d = 0; d < dv; ++d)
+        out[(row * num_qo_heads + head) * dv + d] =
+            M[r] == -INFINITY ? 0.0 : o[(int64_t)r * dv + d] / (kPScale * Z[r]);
+      lse[row * num_qo_heads + head] = M[r] == -INFINITY ? -INFINITY : M[r] + log(Z[r]);
+    }
+done:
+  free(qv);
+  free(s);
+  free(M);
+  free(Z);
+  free(o);
+  free(kr);
+  free(vb);
+  free(limit);
+  return rc;
+}

@@ -118,6 +118,32 @@ int orc_attention_unit(const orc_cache* c, const orc_page_table* pt,
                        int32_t b, int32_t h_kv, int64_t chunk_tokens,
                        double* out, double* lse);
 
+/* Attention with the query and the probabilities quantised to FP4 (page
+ * "fix(attention): correct SM120 NVFP4 qk_correction layout, row-sum
+ * reduction, and lse", description: the SM120 NVFP4 attention it fixes, a
+ * SageAttention3 port, quantises Q, K, V and P to FP4; its row sum carries
+ * the factor 2^fp8_scalexfp4_scale_log2 of the FP4 P quantisation, which lse
+ * drops, and a uniform-score V = ones probe returns the V-quantisation value
+ * 1.031).  The pages print no formula; the readings taken here:
+ *  - each query row is quantised per 16 dims with E4M3 block scales and
+ *    global scale 1 (orc_quantize_block16 with g = 1) and used dequantised;
+ *    no block-mean smoothing (one query token per request and head in
+ *    decode, whose mean is the row itself);
+ *  - p_j = exp(s_j - m), m the row's maximum over all its visible keys (two
+ *    passes: an online kernel's running maximum would tie the codes to its
+ *    tile order), is scaled by 448 * 6 (the E4M3 maximum times the e2m1
+ *    maximum, 2^fp8_scalexfp4_scale_log2) and quantised per 16 consecutive
+ *    key positions 16b .. 16b + 15 with global scale 1 (masked keys count 0);
+ *  - o = sum_j P_hat_j v_hat_j / (448 * 6 * sum_j p_j): the denominator is the
+ *    softmax's own, from the unquantised p; lse = m + ln sum_j p_j.
+ * Arguments and output layout as orc_attention_unit (no split variant). */
+int orc_attention_unit_fp4qp(const orc_cache* c, const orc_page_table* pt,
+                             const int32_t* qo_indptr, const uint16_t* q_bf16,
+                             int64_t q_stride_tok, int64_t q_stride_head,
+                             int32_t num_qo_heads, int32_t causal,
+                             double sm_scale, int32_t b, int32_t h_kv,
+                             double* out, double* lse);
+
 /* Fold n partial states (o_i normalised, lse_i natural log) into one:
  * M = max lse_i; lse = M + ln sum exp(lse_i - M); o = sum exp(lse_i - lse) o_i.
  * All lse_i = -inf (or n = 0) gives o = 0, lse = -inf. */

@@ -91,6 +91,11 @@ def lib():
                 C.c_void_p, C.c_int64, C.c_int64, C.c_int32, C.c_int32,
                 C.c_double, C.c_int32, C.c_int32, C.c_int64, C.c_void_p,
                 C.c_void_p]
+            L.orc_attention_unit_fp4qp.restype = C.c_int
+            L.orc_attention_unit_fp4qp.argtypes = [
+                C.POINTER(OrcCache), C.POINTER(OrcPageTable), C.c_void_p,
+                C.c_void_p, C.c_int64, C.c_int64, C.c_int32, C.c_int32,
+                C.c_double, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]
             L.orc_merge_states.restype = None
             L.orc_merge_states.argtypes = [C.c_int32, C.c_int32, C.c_void_p,
                                            C.c_void_p, C.c_void_p, C.c_void_p]
@@ -257,6 +262,31 @@ def attention(cache: Cache, pt: PageTable, qo_indptr, q, num_qo_heads: int,
                                   chunk_tokens, _ptr(out), _ptr(lse))
         if rc != 0:
             raise RuntimeError("oracle attention failed (%d) for unit %r" % (rc, (b, h)))
+    return out, lse
+
+
+def attention_fp4qp(cache: Cache, pt: PageTable, qo_indptr, q, num_qo_heads: int,
+                    causal: bool, sm_scale: float, units=None, out=None, lse=None):
+    """Attention with the query and the probabilities quantised to FP4
+    (orc_attention_unit_fp4qp); arguments and results as ``attention``."""
+    qo = _np(qo_indptr).astype(np.int32)
+    qb = _np(q)
+    rows = int(qo[-1])
+    Hkv = cache.layout.num_kv_heads
+    if out is None:
+        out = np.full((rows, num_qo_heads, cache.layout.head_dim_vo), np.nan)
+    if lse is None:
+        lse = np.full((rows, num_qo_heads), np.nan)
+    if units is None:
+        units = [(b, h) for b in range(len(qo) - 1) for h in range(Hkv)]
+    L = lib()
+    for b, h in units:
+        rc = L.orc_attention_unit_fp4qp(cache.struct, pt.struct, _ptr(qo), _ptr(qb),
+                                        qb.shape[1] * qb.shape[2], qb.shape[2],
+                                        num_qo_heads, int(causal), sm_scale, b, h,
+                                        _ptr(out), _ptr(lse))
+        if rc != 0:
+            raise RuntimeError("oracle fp4 q/p attention failed (%d) for unit %r" % (rc, (b, h)))
     return out, lse
 
 

@@ -42,6 +42,17 @@ MUTANTS = {
     "page_size_fixed_at_16": (
         "  pidx = pos / c->page_size;\n",
         "  pidx = pos / 16;\n"),
+    "fp4qp_row_sum_without_p_scale": (
+        "o[(int64_t)r * dv + d] / (kPScale * Z[r]);", "o[(int64_t)r * dv + d] / Z[r];"),
+    "fp4qp_p_unquantised": ("      fp4_round16(pp, ph);\n",
+                            "      memcpy(ph, pp, sizeof ph);\n"),
+    "fp4qp_q_unquantised": ("        fp4_round16(x, qv + (int64_t)r * dk + d);\n",
+                            "        memcpy(qv + (int64_t)r * dk + d, x, sizeof x);\n"),
+    "fp4qp_mask_ignored_in_p": ("(j < L && j <= limit[r]) ? kPScale", "(j < L) ? kPScale"),
+    "fp4qp_p_scaled_by_6_only": ("const double kPScale = 448.0 * 6.0;",
+                                 "const double kPScale = 6.0;"),
+    "fp4qp_lse_keeps_p_scale": ("-INFINITY : M[r] + log(Z[r]);",
+                                "-INFINITY : M[r] + log(kPScale * Z[r]);"),
     "kv_len_page_size_fixed_at_16": (
         "  return (np - 1) * page_size + pt->last_page_len[b];",
         "  return (np - 1) * 16 + pt->last_page_len[b];"),

@@ -480,3 +480,121 @@ def test_page_size_one_matches_sixteen(layout):
             a = O.dequant_row(c1, which, int(perm[off[b] + pos]), 0, h)
             r = O.dequant_row(c16, which, int(kvi[kvp[b] + pos // 16]), pos % 16, h)
             assert np.array_equal(a, r)
+
+
+# ---- attention with FP4 query and probabilities ---------------------------
+# Page "fix(attention): correct SM120 NVFP4 qk_correction layout, row-sum
+# reduction, and lse", description: Q, K, V and P quantised to FP4; the row
+# sum carries the FP4 P quantisation factor, which lse drops; the uniform-score
+# V = ones probe returns the V-quantisation value; uniform scores give
+# lse = ln(seq_len).
+
+P_SCALE = 448.0 * 6.0   # E4M3 maximum x e2m1 maximum
+
+
+def fp4_block_values(x):
+    """Exact-real NVFP4 (global scale 1) of 16 values, as values."""
+    packed, sf = exact_block([float(v) for v in x], 1.0)
+    s = O.e4m3_value(sf)
+    vals = []
+    for byte in packed:
+        vals += [O.e2m1_value(byte & 15) * s, O.e2m1_value(byte >> 4) * s]
+    return vals
+
+
+def test_fp4qp_uniform_score_v_ones_probe():
+    gold_v = read_golden("v_ones_probe.txt")
+    gold_l = read_golden("uniform_lse.txt")
+    batch = small_batch((37, 100, 16, 1), qo_len=1)
+    batch.q.zero_()
+    for ts in (batch.prefix, batch.new):
+        ts.v.fill_(1.0)
+    cache, pt = O.cache_from_batch(batch)
+    out, lse = O.attention_fp4qp(cache, pt, batch.qo_indptr, batch.q, 4, False,
+                                 batch.sm_scale)
+    assert np.all(out == gold_v["dequant"])
+    for b, L in enumerate(batch.kv_lens):
+        assert np.all(lse[b] == gold_l[L])
+
+
+def test_fp4qp_reduces_to_exact_attention_when_q_and_p_are_fp4_values():
+    # q = 1.03125 e_0 is its own NVFP4 value (scale E4M3(1.03125/6) = 0.171875,
+    # code 6); K rows k_j = c_j e_0 with c_j in {1.5, 0.75, 0} are their own
+    # NVFP4 values; sm_scale = ln 2 / (1.03125 * 0.75) makes the scores
+    # {2 ln 2, ln 2, 0}, so p in {1, 1/2, 1/4} and 2688 p in {2688, 1344, 672}
+    # = 448 x {6, 3, 1.5}: every quantisation is exact and the method is plain
+    # attention.
+    batch = small_batch((37, 21), qo_len=1, Hq=2, Hkv=1, Dk=32, Dv=32)
+    batch.q.zero_()
+    batch.q[:, :, 0] = 1.03125
+    rng = np.random.default_rng(5)
+    for ts in (batch.prefix, batch.new):
+        ts.k.zero_()
+        ts.k[:, :, 0] = torch.tensor(rng.choice([1.5, 0.75, 0.0], ts.k.shape[0]),
+                                     dtype=torch.bfloat16)[:, None]
+    sm = math.log(2.0) / (1.03125 * 0.75)
+    cache, pt = O.cache_from_batch(batch)
+    ref, ref_lse = O.attention(cache, pt, batch.qo_indptr, batch.q, 2, False, sm)
+    out, lse = O.attention_fp4qp(cache, pt, batch.qo_indptr, batch.q, 2, False, sm)
+    assert np.allclose(out, ref, atol=1e-14, rtol=0)
+    assert np.allclose(lse, ref_lse, atol=1e-14, rtol=0)
+
+
+def test_fp4qp_lse_is_that_of_the_quantised_query():
+    # lse does not depend on P's quantisation: it is the plain log-sum-exp of
+    # the scores of the quantised query.  The quantised query is exact in bf16
+    # (2 + 3 significant bits), so the exact attention of that query gives it,
+    # and quantising the query again changes nothing.
+    batch = small_batch((37, 100, 5), qo_len=2, Hq=4, Hkv=2, Dk=64, Dv=32, causal=True)
+    cache, pt = O.cache_from_batch(batch)
+    qh = batch.q.clone()
+    flat = qh.double().reshape(-1, 16).numpy()
+    qh = torch.tensor(np.array([fp4_block_values(r) for r in flat])).reshape(qh.shape)
+    assert torch.equal(qh.to(torch.bfloat16).double(), qh)
+    qh = qh.to(torch.bfloat16)
+    out1, lse1 = O.attention_fp4qp(cache, pt, batch.qo_indptr, batch.q, 4, True, batch.sm_scale)
+    out2, lse2 = O.attention_fp4qp(cache, pt, batch.qo_indptr, qh, 4, True, batch.sm_scale)
+    _, ref_lse = O.attention(cache, pt, batch.qo_indptr, qh, 4, True, batch.sm_scale)
+    assert np.array_equal(out1, out2) and np.array_equal(lse1, lse2)
+    assert np.allclose(lse1, ref_lse, atol=1e-13, rtol=0)
+
+
+@pytest.mark.parametrize("causal,qo_len", [(False, 1), (True, 3)])
+def test_fp4qp_brute_force_small(causal, qo_len):
+    # every quantisation by the exact rational search over E4M3 and e2m1
+    # values; scores, maxima and sums accumulated in the oracle's order
+    Hq, Hkv, Dk, Dv = 2, 1, 32, 16
+    batch = small_batch((37, 20), qo_len=qo_len, Hq=Hq, Hkv=Hkv, Dk=Dk, Dv=Dv,
+                        causal=causal, seed=23)
+    cache, pt = O.cache_from_batch(batch)
+    out, lse = O.attention_fp4qp(cache, pt, batch.qo_indptr, batch.q, Hq, causal,
+                                 batch.sm_scale)
+    for b, L in enumerate(batch.kv_lens):
+        K, V = dense_kv(cache, pt, b, 0, L)
+        K, V = K.numpy(), V.numpy()
+        for i in range(qo_len):
+            row = b * qo_len + i
+            lim = L - qo_len + i if causal else L - 1
+            for h in range(Hq):
+                x = batch.q[row, h].double().numpy()
+                qv = sum((fp4_block_values(x[k:k + 16]) for k in range(0, Dk, 16)), [])
+                s = []
+                for j in range(L):
+                    acc = 0.0
+                    for d in range(Dk):
+                        acc += qv[d] * K[j, d]
+                    s.append(batch.sm_scale * acc)
+                m = max(s[:lim + 1])
+                z = 0.0
+                for j in range(lim + 1):
+                    z += math.exp(s[j] - m)
+                o = np.zeros(Dv)
+                for blk in range(0, L, 16):
+                    pp = [P_SCALE * math.exp(s[j] - m) if j < L and j <= lim else 0.0
+                          for j in range(blk, blk + 16)]
+                    ph = fp4_block_values(pp)
+                    for t in range(16):
+                        if blk + t < L:
+                            o += ph[t] * V[blk + t]
+                assert np.allclose(out[row, h], o / (P_SCALE * z), atol=1e-13, rtol=0)
+                assert lse[row, h] == pytest.approx(m + math.log(z), abs=1e-13)
