@@ -407,7 +407,9 @@ def run_gpu(args, world, rank, local):
                    "none": "not flushed (profiler capture; not a timing)"}[args.l2_flush],
             "kernel": {1: "tensor-core mma.sync f16/f32acc",
                        2: "CUDA-core f32",
-                       3: "tcgen05.mma f16/f32acc, K_hat in tensor memory"}[plan.info.kernel],
+                       3: "tcgen05.mma f16/f32acc, K_hat in tensor memory",
+                       4: "FP4 query and probabilities: row-maximum launch + mma.sync "
+                          "attention launch, FP4 operands expanded exactly to f16"}[plan.info.kernel],
             "split_units": int(plan.info.num_units), "split": int(plan.info.split),
             "chunk_pages": int(plan.info.chunk_pages),
             "us_per_call": ms_step_max * 1e3,
@@ -423,11 +425,13 @@ def run_gpu(args, world, rank, local):
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": peak_kind},
         "e2e": e2e,
-        "gpu_launches": args.steps * (2 if args.separate_append else 1),
+        "gpu_launches": args.steps * ((2 if args.separate_append else 1) +
+                                      (1 if plan.info.kernel == 4 else 0)),
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(batch, args.layout)
+        result["cpu_baseline"] = cpu_baseline(batch, args.layout,
+                                              fp4qp=plan.info.kernel == 4)
     return result
 
 
@@ -532,9 +536,10 @@ def _oracle_prefix_cache(batch, requests, layout):
     return c, pt
 
 
-def _oracle_units(O, cache, pt, batch, units, threads, chunk=None):
+def _oracle_units(O, cache, pt, batch, units, threads, chunk=None, fp4qp=False):
     """Oracle step on (request, kv head) units: append the requests' new
-    tokens, then exact attention, the units spread over a thread pool
+    tokens, then exact attention (or, with fp4qp, the FP4 query and
+    probabilities method of kernel 4), the units spread over a thread pool
     (ctypes releases the GIL)."""
     import concurrent.futures as cf
     c = batch.cfg
@@ -547,10 +552,11 @@ def _oracle_units(O, cache, pt, batch, units, threads, chunk=None):
     import numpy as np
     out = np.full((rows, c.num_qo_heads, c.head_dim_vo), np.nan)
     lse = np.full((rows, c.num_qo_heads), np.nan)
+    fn = O.attention_fp4qp if fp4qp else O.attention
     with cf.ThreadPoolExecutor(max_workers=threads) as ex:
-        list(ex.map(lambda u: O.attention(cache, pt, batch.qo_indptr, batch.q,
-                                          c.num_qo_heads, c.causal, batch.sm_scale,
-                                          units=[u], out=out, lse=lse), units))
+        list(ex.map(lambda u: fn(cache, pt, batch.qo_indptr, batch.q, c.num_qo_heads,
+                                 c.causal, batch.sm_scale, units=[u], out=out, lse=lse),
+                    units))
     return out, lse
 
 
@@ -572,17 +578,17 @@ def cpu_model() -> str:
     return "unknown"
 
 
-def _timed_passes(O, cache, pt, batch, units, threads, min_s, max_passes):
+def _timed_passes(O, cache, pt, batch, units, threads, min_s, max_passes, fp4qp=False):
     passes, t0 = 0, time.perf_counter()
     while True:
-        _oracle_units(O, cache, pt, batch, units, threads)
+        _oracle_units(O, cache, pt, batch, units, threads, fp4qp=fp4qp)
         passes += 1
         dt = time.perf_counter() - t0
         if dt >= min_s or passes >= max_passes:
             return passes, dt
 
 
-def cpu_baseline(batch, layout, min_s: float = 10.0, max_passes: int = 100):
+def cpu_baseline(batch, layout, min_s: float = 10.0, max_passes: int = 100, fp4qp=False):
     """The oracle as it stands on the host cores: up to 4 requests of the
     workload, one (request, kv head) unit per thread on all cores (whole
     passes repeated for about ``min_s`` seconds, at most ``max_passes``), and
@@ -594,17 +600,19 @@ def cpu_baseline(batch, layout, min_s: float = 10.0, max_passes: int = 100):
     cache, pt = _oracle_prefix_cache(batch, requests, layout)
     units = [(b, h) for b in requests for h in range(c.num_kv_heads)]
     threads = min(len(units), cores)
-    passes, dt = _timed_passes(O, cache, pt, batch, units, threads, min_s, max_passes)
+    passes, dt = _timed_passes(O, cache, pt, batch, units, threads, min_s, max_passes, fp4qp)
     toks = sum(batch.kv_lens[b] for b in requests)
-    p1, dt1 = _timed_passes(O, cache, pt, batch, [(0, 0)], 1, min_s / 3, max_passes)
+    p1, dt1 = _timed_passes(O, cache, pt, batch, [(0, 0)], 1, min_s / 3, max_passes, fp4qp)
     return {"value": toks * passes / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
             "cpu_count": cores, "cpu_model": cpu_model(),
             "value_1core": batch.kv_lens[0] / c.num_kv_heads * p1 / dt1,
             "sample": "requests %s of the workload (%d KV tokens x %d kv heads), append of "
-                      "their new tokens + float64 exact attention, one (request, kv head) "
+                      "their new tokens + float64 %s, one (request, kv head) "
                       "unit per thread on %d threads, %d passes in %.1f s; value_1core: "
                       "request 0, kv head 0 on one thread, %d passes in %.1f s" % (
-                          requests, toks, c.num_kv_heads, threads, passes, dt, p1, dt1)}
+                          requests, toks, c.num_kv_heads,
+                          "FP4 query and probabilities attention" if fp4qp else
+                          "exact attention", threads, passes, dt, p1, dt1)}
 
 
 def run_reference(args, world, rank):
@@ -626,7 +634,7 @@ def run_reference(args, world, rank):
     # and reports the steps it timed.
     budget = float(os.environ.get("NVFP4KV_REF_BUDGET_S", "150"))
     t0 = time.perf_counter()
-    _oracle_units(O, cache, pt, batch, all_units[:1], 1)
+    _oracle_units(O, cache, pt, batch, all_units[:1], 1, fp4qp=args.kernel == 4)
     unit_s = time.perf_counter() - t0
     per_step = budget / max(1, args.steps + args.warmup)
     n_units = max(1, min(len(all_units), int(per_step / max(unit_s, 1e-9) * cores)))
@@ -636,7 +644,7 @@ def run_reference(args, world, rank):
     start = time.perf_counter()
     for k in range(args.warmup + args.steps):
         t = time.perf_counter()
-        _oracle_units(O, cache, pt, batch, units, threads)
+        _oracle_units(O, cache, pt, batch, units, threads, fp4qp=args.kernel == 4)
         if k >= args.warmup:
             times.append(time.perf_counter() - t)
         if len(times) >= 3 and time.perf_counter() - start > budget:
@@ -668,7 +676,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="long_context_decode", choices=list(W.WORKLOADS))
     ap.add_argument("--layout", default="HND", choices=["HND", "NHD"])
-    ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 tensor-core mma.sync, 2 CUDA-core, 3 tcgen05")
+    ap.add_argument("--kernel", type=int, default=0,
+                    help="0 auto, 1 tensor-core mma.sync, 2 CUDA-core, 3 tcgen05, "
+                         "4 FP4 query and probabilities")
     ap.add_argument("--chunk-tokens", type=int, default=0,
                     help="split-KV chunk in tokens (multiple of 16); 0 = the planner's choice")
     ap.add_argument("--no-cpu-baseline", action="store_true")

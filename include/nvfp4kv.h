@@ -152,7 +152,20 @@ typedef struct nvfp4kv_plan_options {
   int32_t kernel;             /* 0 auto (3 when head dims are 128 and a kv
                                  head has more than 16 query rows, else 1),
                                  1 tensor-core (mma.sync), 2 CUDA-core,
-                                 3 tcgen05 (head dims 128 x 128 only)      */
+                                 3 tcgen05 (head dims 128 x 128 only),
+                                 4 FP4 query and probabilities: the query
+                                 quantised to NVFP4 per 16 dims, p = exp(s
+                                 - m) against the row's maximum over all its
+                                 keys (a first launch computes the maxima),
+                                 scaled by 448 * 6 and quantised to NVFP4
+                                 per 16 consecutive keys before the PV
+                                 product; o divides by that scale times the
+                                 unquantised sum of p, lse is the plain
+                                 ln-sum-exp (page "fix(attention): correct
+                                 SM120 NVFP4 qk_correction layout, row-sum
+                                 reduction, and lse", description).  At most
+                                 8 query rows per kv head; mma.sync with the
+                                 FP4 operands expanded exactly to f16      */
   int32_t num_sms;            /* >0: override the device's SM count          */
   int32_t ctas_per_sm;        /* >0: override the occupancy query            */
   int32_t out_dtype;          /* output element: 0 bf16 (default), 1 f16      */
@@ -169,7 +182,8 @@ typedef struct nvfp4kv_plan_info {
   uint32_t magic;
   int32_t batch, num_qo_heads, num_kv_heads, head_dim_qk, head_dim_vo;
   int32_t page_size, causal;
-  int32_t kernel;          /* 1 tensor-core, 2 CUDA-core, 3 tcgen05          */
+  int32_t kernel;          /* 1 tensor-core, 2 CUDA-core, 3 tcgen05, 4 FP4
+                              query and probabilities (two launches)       */
   int32_t num_units;       /* attention work units (grid x)                  */
   int32_t row_blocks;      /* query-row blocks per unit (grid y)             */
   int32_t rows_per_block;  /* query rows (G x qo positions) per CTA          */
@@ -188,6 +202,8 @@ typedef struct nvfp4kv_plan_info {
       off_partial_o;       /* byte offsets inside the workspace              */
   uint64_t off_counters;   /* merge arrival counters (self-resetting)        */
   const int32_t* device_last_page_len;  /* the plan option, or NULL          */
+  uint64_t off_row_max;    /* kernel 4: f32 row maxima [rows][Hq][units per
+                              request] written by the first launch (else 0) */
 } nvfp4kv_plan_info;
 
 /* Build the plan from HOST copies of the batch description.

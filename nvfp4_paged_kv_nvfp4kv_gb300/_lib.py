@@ -59,7 +59,7 @@ class PlanInfo(C.Structure):
         (n, C.c_uint64) for n in (
             "workspace_bytes", "plan_host_bytes", "off_flags", "off_units",
             "off_merge_indptr", "off_partial_lse", "off_partial_o", "off_counters")] + [
-        ("device_last_page_len", C.c_void_p)]
+        ("device_last_page_len", C.c_void_p), ("off_row_max", C.c_uint64)]
 
 
 _vp, _i32, _i64, _u64, _f32 = C.c_void_p, C.c_int32, C.c_int64, C.c_uint64, C.c_float

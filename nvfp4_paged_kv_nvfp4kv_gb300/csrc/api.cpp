@@ -22,6 +22,7 @@ bool attend_config_tc(int dk, int dv, int rows, AttendConfig* cfg);
 bool attend_config_simt(int dk, int dv, int rows, AttendConfig* cfg);
 bool attend_config_tcgen05(int dk, int dv, int rows, AttendConfig* cfg);
 bool attend_config_dec(int dk, int dv, int rows, int quads, AttendConfig* cfg);
+bool attend_config_tc_fp4qp(int dk, int dv, int rows, int pass, AttendConfig* cfg);
 cudaError_t prepare_kernel(const AttendConfig& cfg);
 }  // namespace nvfp4kv
 
@@ -141,6 +142,7 @@ bool lookup_kernel(int kind, int dk, int dv, int rows, AttendConfig* cfg) {
   if (kind == kKernelTensorCore) return attend_config_tc(dk, dv, rows, cfg);
   if (kind == kKernelCudaCore) return attend_config_simt(dk, dv, rows, cfg);
   if (kind == kKernelTcgen05) return attend_config_tcgen05(dk, dv, rows, cfg);
+  if (kind == kKernelFp4QP) return attend_config_tc_fp4qp(dk, dv, rows, 2, cfg);
   return false;
 }
 
@@ -299,7 +301,7 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
                 "force_chunk_tokens %d must be a non-negative multiple of 16",
                 opts.force_chunk_tokens);
   if (opts.max_splits < 0 || opts.num_sms < 0 || opts.ctas_per_sm < 0 || opts.kernel < 0 ||
-      opts.kernel > 3)
+      opts.kernel > 4)
     return fail(NVFP4KV_ERR_INVALID_ARGUMENT, "bad plan option");
   const int G = num_qo_heads / num_kv_heads;
 
@@ -353,11 +355,14 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
                                                                        : kKernelTensorCore;
   const int want_rows = kind == kKernelTcgen05 ? std::max(max_rows, 1) : (max_rows <= 8 ? 8 : 16);
   if (!lookup_kernel(kind, head_dim_qk, head_dim_vo, want_rows, &cfg))
-    return fail(NVFP4KV_ERR_UNSUPPORTED, "no %s kernel for head dims (%d, %d)",
+    return fail(NVFP4KV_ERR_UNSUPPORTED, "no %s kernel for head dims (%d, %d)%s",
                 kind == kKernelTensorCore ? "tensor-core"
                 : kind == kKernelTcgen05  ? "tcgen05"
+                : kind == kKernelFp4QP    ? "FP4 query/probability"
                                           : "CUDA-core",
-                head_dim_qk, head_dim_vo);
+                head_dim_qk, head_dim_vo,
+                kind == kKernelFp4QP && want_rows > 8 ? " and more than 8 query rows per kv head"
+                                                      : "");
   const int rows_per_block = cfg.rows;
   // A tensor-core plan of one block of <= 8 rows at page size 16 runs the
   // decode kernel where the cache layout allows it; that kernel takes several
@@ -522,7 +527,11 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
   const uint64_t off_merge = align_up(off_units + units.size() * sizeof(WorkUnit), 256);
   const uint64_t off_plse = align_up(off_merge + (split ? (entries + 1) * 4 : 0), 256);
   const uint64_t off_po = align_up(off_plse + partial * 4, 256);
-  const uint64_t ws_bytes = align_up(off_po + (uint64_t)partial * head_dim_vo * 4, 256);
+  const uint64_t off_rm = align_up(off_po + (uint64_t)partial * head_dim_vo * 4, 256);
+  const uint64_t n_row_max = kind == kKernelFp4QP
+                                 ? (uint64_t)total_rows * num_qo_heads * std::max(max_units, 1)
+                                 : 0;
+  const uint64_t ws_bytes = align_up(off_rm + n_row_max * 4, 256);
   const uint64_t host_bytes = off_plse - off_units;
 
   info->magic = kPlanMagic;
@@ -556,6 +565,7 @@ int nvfp4kv_decode_plan(const int32_t* qo_indptr_h, const int32_t* kv_indptr_h,
   info->off_partial_lse = off_plse;
   info->off_partial_o = off_po;
   info->off_counters = off_counters;
+  info->off_row_max = n_row_max ? off_rm : 0;
   info->device_last_page_len = opts.device_last_page_len;
 
   if (host_bytes > 0 && (!plan_host || plan_host_bytes < host_bytes))
@@ -651,7 +661,8 @@ int attend(const nvfp4kv_plan_info* info, const void* q_bf16, int64_t q_stride_t
                          workspace, workspace_bytes, out_bf16))
     return st;
   if (nt) {
-    if (info->kernel != kKernelTensorCore && info->kernel != kKernelTcgen05)
+    if (info->kernel != kKernelTensorCore && info->kernel != kKernelTcgen05 &&
+        info->kernel != kKernelFp4QP)
       return fail(NVFP4KV_ERR_UNSUPPORTED, "the fused append runs in the tensor-core kernels");
     if (info->num_units > 0 &&
         (!nt->k || !nt->v || !aligned(nt->k, 16) || !aligned(nt->v, 16) ||
@@ -710,6 +721,22 @@ int attend(const nvfp4kv_plan_info* info, const void* q_bf16, int64_t q_stride_t
     p.nv_stride_head = nt->v_stride_head;
     p.k_global_scale = cache->k_global_scale;
     p.v_global_scale = cache->v_global_scale;
+  }
+  if (info->kernel == kKernelFp4QP) {
+    // FP4 query and probabilities: the row-maximum pass (which also stores
+    // the fused append's tokens), then the attention pass with those maxima
+    AttendConfig mcfg{};
+    if (!attend_config_tc_fp4qp(info->head_dim_qk, info->head_dim_vo, info->rows_per_block, 1,
+                                &mcfg))
+      return fail(NVFP4KV_ERR_UNSUPPORTED, "planned kernel not available");
+    e = prepare_kernel(mcfg);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel attributes");
+    p.row_max = reinterpret_cast<float*>(ws + info->off_row_max);
+    p.row_max_splits = std::max(info->max_units_per_request, 1);
+    e = launch_attend(mcfg, p, info->num_units, info->row_blocks, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "row-maximum launch");
+    p.new_k = nullptr;
+    p.new_v = nullptr;
   }
   e = launch_attend(cfg, p, info->num_units, info->row_blocks, stream);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");

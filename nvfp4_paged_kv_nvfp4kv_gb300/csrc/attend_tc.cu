@@ -39,6 +39,24 @@
 //    the lanes that hold one row.  Warps combine through shared memory; the
 //    unit writes bf16 out + lse, or an f32 partial state + lse for the merge
 //    when the plan split the request.
+//
+// FP4 query and probabilities (kernel 4; page "fix(attention): correct SM120
+// NVFP4 qk_correction layout, row-sum reduction, and lse", description: the
+// SageAttention3-style NVFP4 attention quantises Q and P to FP4 and its row
+// sum carries the factor of the FP4 P quantisation, which lse drops), one
+// block of <= 8 rows, two launches of this kernel:
+//  * MODE 1 quantises each 16-dim block of Q to NVFP4 (global scale 1, the
+//    cache's exact recipe), takes the scores like MODE 0 and stores each
+//    unit's row maxima (no V, no PV);
+//  * MODE 2 reads the maxima of all units of the request, takes p = 2^(x -
+//    m) (m the row's maximum over all its keys), and per row and 16-token
+//    tile quantises 2688 p to NVFP4: E4M3 scale RN(max / 6), e2m1 codes by
+//    exact comparisons with midpoint x scale; code x scale is exact in f16,
+//    so the mma.sync PV product takes exactly the block-scaled FP4 operand.
+//    The row sum is that of the unquantised p times 2688, the maximum
+//    m - log2(2688), so the common epilogue writes o = sum P_hat v_hat /
+//    (2688 sum p) and lse = ln sum exp(s).
+
 #include <cfloat>
 #include <cstdint>
 #include <type_traits>
@@ -49,6 +67,7 @@
 #include "device_common.cuh"
 #include "append_fused.cuh"
 #include "internal.h"
+#include "quantize.cuh"
 #include "epilogue.cuh"
 #include "stage.cuh"
 
@@ -97,10 +116,28 @@ constexpr int tc_min_blocks() {
 // by more than this (log2 domain), so p <= 2^kRaiseLog2 fits f16.
 constexpr float kRaiseLog2 = 8.f;
 
-template <int DK, int DV, int NT, int WARPS, int STAGES>
+// FP4 query and probabilities (MODE 1: the row-maximum pass, MODE 2: the
+// attention pass).  p is scaled by the E4M3 maximum times the e2m1 maximum
+// before its NVFP4 quantisation, so a block holding the row's maximum gets
+// the scale 448.
+constexpr float kPScale = 448.f * 6.f;
+constexpr float kLog2PScale = 11.392317422778760f;  // log2(2688)
+
+// e2m1 code (0..7) of x / sc, x >= 0, round to nearest, ties to the even
+// code, saturating at 6: x is compared with the midpoints between adjacent
+// values times the scale (th[k] = {0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5}[k] *
+// sc, exact products), and a tie goes up only where the upper code is even.
+__device__ __forceinline__ uint32_t e2m1_code_of(float x, const float (&th)[7]) {
+  return (uint32_t)(x > th[0]) + (uint32_t)(x >= th[1]) + (uint32_t)(x > th[2]) +
+         (uint32_t)(x >= th[3]) + (uint32_t)(x > th[4]) + (uint32_t)(x >= th[5]) +
+         (uint32_t)(x > th[6]);
+}
+
+template <int DK, int DV, int NT, int WARPS, int STAGES, int MODE>
 __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
     attend_tc_kernel(const AttendParams p) {
   using T = TcTraits<DK, DV, NT, WARPS, STAGES>;
+  static_assert(MODE == 0 || NT == 1, "FP4 query and probabilities: one row block");
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* pipe = smem;
   uint16_t* sQ = reinterpret_cast<uint16_t*>(smem + T::MAIN_BYTES);
@@ -192,57 +229,93 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
   }
   int32_t next_pid = page_id(STAGES - 1);
 
-  // ---- Q: per-row power-of-two prescale into f16, row limits ------------
-  // amax of each row (non-negative floats order like their bit patterns)
   __syncthreads();  // the amax slots are zeroed; late appended tokens stored
+  if constexpr (MODE == 0) {
+    // ---- Q: per-row power-of-two prescale into f16, row limits ----------
+    // amax of each row (non-negative floats order like their bit patterns)
 #pragma unroll
-  for (int k = 0; k < QPT; ++k) {
-    const int ci = tid + k * WARPS * 32;
-    if (ci >= QCH) continue;
-    const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
-    float am = 0.f;
+    for (int k = 0; k < QPT; ++k) {
+      const int ci = tid + k * WARPS * 32;
+      if (ci >= QCH) continue;
+      const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
+      float am = 0.f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      am = fmaxf(am, fmaxf(fabsf(bf16_bits_to_f32(w[j] & 0xFFFFu)),
-                           fabsf(bf16_bits_to_f32(w[j] >> 16))));
-    atomicMax(reinterpret_cast<int*>(sRowF) + ci / (DK / 8), __float_as_int(am));
-  }
-  __syncthreads();
-#pragma unroll
-  for (int k = 0; k < QPT; ++k) {
-    const int ci = tid + k * WARPS * 32;
-    if (ci >= QCH) continue;
-    const int rr = ci / (DK / 8);
-    const float amax = __int_as_float(reinterpret_cast<const int*>(sRowF)[rr]);
-    // e such that amax * 2^e lies in [2^14, 2^15)
-    int e = 0;
-    if (amax > 0.f) e = 14 - (int)((__float_as_uint(amax) >> 23) & 0xFF) + 127;
-    e = max(-120, min(120, e));
-    const float up = __uint_as_float((uint32_t)(127 + e) << 23);
-    const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
-    uint32_t h[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      h[j] = f32x2_to_f16x2(bf16_bits_to_f32(w[j] & 0xFFFFu) * up,
-                            bf16_bits_to_f32(w[j] >> 16) * up);
-    *reinterpret_cast<uint4*>(sQ + rr * T::QROW + (ci % (DK / 8)) * 8) =
-        make_uint4(h[0], h[1], h[2], h[3]);
-    if (ci % (DK / 8) == 0) {
-      const int r = row0 + rr;
-      sRowLim[rr] = r >= R ? -1 : (p.causal ? (u.kv_len - u.qo_len + r / G) : (u.kv_len - 1));
-      // the row factor replaces the amax slot once every thread has read it
-      qv[k].x = __float_as_uint(r >= R ? 0.f
-                                       : p.qk_scale_log2 *
-                                             __uint_as_float((uint32_t)(127 - e) << 23));
+      for (int j = 0; j < 4; ++j)
+        am = fmaxf(am, fmaxf(fabsf(bf16_bits_to_f32(w[j] & 0xFFFFu)),
+                             fabsf(bf16_bits_to_f32(w[j] >> 16))));
+      atomicMax(reinterpret_cast<int*>(sRowF) + ci / (DK / 8), __float_as_int(am));
     }
-  }
-  __syncthreads();
+    __syncthreads();
 #pragma unroll
-  for (int k = 0; k < QPT; ++k) {
-    const int ci = tid + k * WARPS * 32;
-    if (ci < QCH && ci % (DK / 8) == 0) sRowF[ci / (DK / 8)] = __uint_as_float(qv[k].x);
+    for (int k = 0; k < QPT; ++k) {
+      const int ci = tid + k * WARPS * 32;
+      if (ci >= QCH) continue;
+      const int rr = ci / (DK / 8);
+      const float amax = __int_as_float(reinterpret_cast<const int*>(sRowF)[rr]);
+      // e such that amax * 2^e lies in [2^14, 2^15)
+      int e = 0;
+      if (amax > 0.f) e = 14 - (int)((__float_as_uint(amax) >> 23) & 0xFF) + 127;
+      e = max(-120, min(120, e));
+      const float up = __uint_as_float((uint32_t)(127 + e) << 23);
+      const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
+      uint32_t h[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        h[j] = f32x2_to_f16x2(bf16_bits_to_f32(w[j] & 0xFFFFu) * up,
+                              bf16_bits_to_f32(w[j] >> 16) * up);
+      *reinterpret_cast<uint4*>(sQ + rr * T::QROW + (ci % (DK / 8)) * 8) =
+          make_uint4(h[0], h[1], h[2], h[3]);
+      if (ci % (DK / 8) == 0) {
+        const int r = row0 + rr;
+        sRowLim[rr] = r >= R ? -1 : (p.causal ? (u.kv_len - u.qo_len + r / G) : (u.kv_len - 1));
+        // the row factor replaces the amax slot once every thread has read it
+        qv[k].x = __float_as_uint(r >= R ? 0.f
+                                         : p.qk_scale_log2 *
+                                               __uint_as_float((uint32_t)(127 - e) << 23));
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < QPT; ++k) {
+      const int ci = tid + k * WARPS * 32;
+      if (ci < QCH && ci % (DK / 8) == 0) sRowF[ci / (DK / 8)] = __uint_as_float(qv[k].x);
+    }
+    __syncthreads();
+  } else {
+    // ---- Q quantised to NVFP4 (global scale 1) with the cache's exact
+    // recipe, used as its f16 values (code x E4M3 scale is exact in f16).
+    // The two 8-dim chunks of a 16-dim block sit in lanes 2m and 2m + 1,
+    // which trade halves so that each quantises the whole block.
+    static_assert((DK / 8) % 2 == 0 && (WARPS * 32) % 2 == 0, "block pairs");
+#pragma unroll
+    for (int k = 0; k < QPT; ++k) {
+      const int ci = tid + k * WARPS * 32;
+      const uint4 mine = qv[k];
+      uint4 other;
+      other.x = __shfl_xor_sync(0xffffffffu, mine.x, 1);
+      other.y = __shfl_xor_sync(0xffffffffu, mine.y, 1);
+      other.z = __shfl_xor_sync(0xffffffffu, mine.z, 1);
+      other.w = __shfl_xor_sync(0xffffffffu, mine.w, 1);
+      const bool odd = ci & 1;
+      uint2 packed;
+      const uint32_t sfb = quantize_block16(odd ? other : mine, odd ? mine : other, 1.0f, &packed);
+      const uint32_t sc = bcast_lo(e4m3x2_to_f16x2(sfb));
+      uint32_t h[4];
+      e2m1x8_to_f16x8(odd ? packed.y : packed.x, h);
+      if (ci >= QCH) continue;
+      const int rr = ci / (DK / 8);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) h[j] = hmul2(h[j], sc);
+      *reinterpret_cast<uint4*>(sQ + rr * T::QROW + (ci % (DK / 8)) * 8) =
+          make_uint4(h[0], h[1], h[2], h[3]);
+      if (ci % (DK / 8) == 0) {
+        const int r = row0 + rr;
+        sRowLim[rr] = r >= R ? -1 : (p.causal ? (u.kv_len - u.qo_len + r / G) : (u.kv_len - 1));
+        sRowF[rr] = r >= R ? 0.f : p.qk_scale_log2;
+      }
+    }
+    __syncthreads();
   }
-  __syncthreads();
 
   // per-lane row data: rows g (half 0) and g + 8 (half 1)
   float rowf[NT];
@@ -293,6 +366,22 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
     for (int kk = 0; kk < T::KSTEPS; ++kk) q_frag(kk, qreg[kk]);
   }
 
+  // FP4 query and probabilities: MODE 1 keeps this lane's maxima of its rows'
+  // scores; MODE 2 reads each row's maximum over every unit of its request
+  // (written by MODE 1 in the previous launch)
+  float mfix[2] = {-INFINITY, -INFINITY};
+  if constexpr (MODE == 2) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int r = row0 + 2 * t + k;
+      if (lim2[k] >= 0) {
+        const float* rm = p.row_max + ((int64_t)(u.qo_begin + r / G) * p.num_qo_heads +
+                                       u.h_kv * G + r % G) * p.row_max_splits;
+        for (int sp = 0; sp < u.num_splits; ++sp) mfix[k] = fmaxf(mfix[k], rm[sp]);
+      }
+    }
+  }
+
   // ---- per-warp state --------------------------------------------------
   float m_run[NT], l_run[NT];
   float oacc[T::MT][NT][4];
@@ -331,7 +420,7 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
     constexpr int VW = T::VC / 4 > 0 ? T::VC / 4 : 1;  // 32-bit words per lane
     uint32_t vw[4][VW];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < (MODE == 1 ? 0 : 4); ++k) {
       const uint8_t* src = vrow + tk[k] * T::VROW;
       if constexpr (T::VC == 16) {
         const uint4 v = *reinterpret_cast<const uint4*>(src);
@@ -351,7 +440,7 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
     constexpr int NBL = (T::VC * 2 + 15) / 16;
     uint32_t sA[NBL], sB[NBL];
 #pragma unroll
-    for (int bl = 0; bl < NBL; ++bl) {
+    for (int bl = 0; bl < (MODE == 1 ? 0 : NBL); ++bl) {
       const int blk = (g * T::VC * 2) / 16 + bl;
       const uint8_t* sfs = st + T::OFF_VSF + blk;
       uint32_t s0 = sfs[tk[0] * T::VSFROW], s1 = sfs[tk[1] * T::VSFROW];
@@ -438,46 +527,87 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
         if (tb > lim2[0]) x[2] = -INFINITY;
         if (tb > lim2[1]) x[3] = -INFINITY;
       }
-      const bool trig = (x[0] > thr2[0]) | (x[2] > thr2[0]) | (x[1] > thr2[1]) | (x[3] > thr2[1]);
-      if (__any_sync(0xffffffffu, trig)) {
-        // raise each row's maximum to this page's exact maximum (a row's
-        // values sit in the 8 lanes of the same t)
-        float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
+      if constexpr (MODE == 1) {
+        // the row-maximum pass: this lane's maxima of rows 2t, 2t+1
+        mfix[0] = fmaxf(mfix[0], fmaxf(x[0], x[2]));
+        mfix[1] = fmaxf(mfix[1], fmaxf(x[1], x[3]));
+      } else if constexpr (MODE == 2) {
+        // p against the row's maximum over all its keys, scaled by 448 * 6;
+        // per row, the page's 16 values (the 8 lanes of the same t) share an
+        // E4M3 scale RN(max / 6) and each becomes an e2m1 value times it
+        float pp[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          pp[k] = mfix[k & 1] == -INFINITY ? 0.f : ex2(x[k] - mfix[k & 1]);
+        lrow[0] += pp[0] + pp[2];
+        lrow[1] += pp[1] + pp[3];
+        float bm[2] = {fmaxf(pp[0], pp[2]) * kPScale, fmaxf(pp[1], pp[3]) * kPScale};
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
-          mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], o));
-          mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], o));
+          bm[0] = fmaxf(bm[0], __shfl_xor_sync(0xffffffffu, bm[0], o));
+          bm[1] = fmaxf(bm[1], __shfl_xor_sync(0xffffffffu, bm[1], o));
         }
-        float corr[2] = {1.f, 1.f};
+        unsigned short sc8;  // E4M3 scales: row 2t low byte, row 2t + 1 high
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n"
+            : "=h"(sc8) : "f"(__fdiv_rn(bm[1], 6.f)), "f"(__fdiv_rn(bm[0], 6.f)));
+        const uint32_t sch = e4m3x2_to_f16x2(sc8);
+        constexpr float kMid[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.f};
+        uint32_t code[4];
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-          if (mx[k] != -INFINITY && (mrow[k] == -INFINITY || mx[k] > 0.f)) {
-            if (mrow[k] != -INFINITY) corr[k] = ex2(-mx[k]);  // 2^(m_old - m_new)
-            mrow[k] = (mrow[k] == -INFINITY ? 0.f : mrow[k]) + mx[k];
-            nm2[k] = -mrow[k];
-            thr2[k] = kRaiseLog2;
-            x[k] -= mx[k];
-            x[k + 2] -= mx[k];
-          }
-          lrow[k] *= corr[k];
-        }
-        if (corr[0] != 1.f || corr[1] != 1.f) {
+          const float scf =
+              __half2float(__ushort_as_half((unsigned short)(k ? sch >> 16 : sch & 0xFFFFu)));
+          float th[7];
 #pragma unroll
-          for (int mt = 0; mt < T::MT; ++mt) {
-            oacc[mt][0][0] *= corr[0];
-            oacc[mt][0][1] *= corr[1];
-            oacc[mt][0][2] *= corr[0];
-            oacc[mt][0][3] *= corr[1];
+          for (int m = 0; m < 7; ++m) th[m] = kMid[m] * scf;
+          code[k] = scf > 0.f ? e2m1_code_of(pp[k] * kPScale, th) : 0u;
+          code[k + 2] = scf > 0.f ? e2m1_code_of(pp[k + 2] * kPScale, th) : 0u;
+        }
+        // e2m1 value x E4M3 scale is exact in f16 (at most 2688)
+        pfrag[0][0] = movmatrix_trans(hmul2(e2m1x2_byte_to_f16x2<0>(code[0] | code[1] << 4), sch));
+        pfrag[0][1] = movmatrix_trans(hmul2(e2m1x2_byte_to_f16x2<0>(code[2] | code[3] << 4), sch));
+      } else {
+        const bool trig = (x[0] > thr2[0]) | (x[2] > thr2[0]) | (x[1] > thr2[1]) | (x[3] > thr2[1]);
+        if (__any_sync(0xffffffffu, trig)) {
+          // raise each row's maximum to this page's exact maximum (a row's
+          // values sit in the 8 lanes of the same t)
+          float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) {
+            mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], o));
+            mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], o));
+          }
+          float corr[2] = {1.f, 1.f};
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            if (mx[k] != -INFINITY && (mrow[k] == -INFINITY || mx[k] > 0.f)) {
+              if (mrow[k] != -INFINITY) corr[k] = ex2(-mx[k]);  // 2^(m_old - m_new)
+              mrow[k] = (mrow[k] == -INFINITY ? 0.f : mrow[k]) + mx[k];
+              nm2[k] = -mrow[k];
+              thr2[k] = kRaiseLog2;
+              x[k] -= mx[k];
+              x[k + 2] -= mx[k];
+            }
+            lrow[k] *= corr[k];
+          }
+          if (corr[0] != 1.f || corr[1] != 1.f) {
+#pragma unroll
+            for (int mt = 0; mt < T::MT; ++mt) {
+              oacc[mt][0][0] *= corr[0];
+              oacc[mt][0][1] *= corr[1];
+              oacc[mt][0][2] *= corr[0];
+              oacc[mt][0][3] *= corr[1];
+            }
           }
         }
+        const float p0 = ex2(x[0]), p1 = ex2(x[1]), p2 = ex2(x[2]), p3 = ex2(x[3]);
+        lrow[0] += p0 + p2;
+        lrow[1] += p1 + p3;
+        // P^T fragments for the PV product: transpose the two 8 x 8 blocks
+        // (tokens 0-7 and 8-15 x the 8 rows)
+        pfrag[0][0] = movmatrix_trans(f32x2_to_f16x2(p0, p1));
+        pfrag[0][1] = movmatrix_trans(f32x2_to_f16x2(p2, p3));
       }
-      const float p0 = ex2(x[0]), p1 = ex2(x[1]), p2 = ex2(x[2]), p3 = ex2(x[3]);
-      lrow[0] += p0 + p2;
-      lrow[1] += p1 + p3;
-      // P^T fragments for the PV product: transpose the two 8 x 8 blocks
-      // (tokens 0-7 and 8-15 x the 8 rows)
-      pfrag[0][0] = movmatrix_trans(f32x2_to_f16x2(p0, p1));
-      pfrag[0][1] = movmatrix_trans(f32x2_to_f16x2(p2, p3));
     } else {
       // ---- S = Q K^T for tokens tok0 .. tok0+15 (two n-tiles) -------------
       // two accumulators per n-tile (alternate k-steps) halve the dependent
@@ -593,7 +723,7 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
 
     // ---- O^T += V_hat^T P^T ---------------------------------------------
     // tokens 2t, 2t+1, 2t+8, 2t+9; lane group g owns bytes [g*VC, g*VC+VC)
-    {
+    if constexpr (MODE != 1) {
       // Interleave the nibbles of two tokens' bytes before converting: for
       // words W0 (token 2t) and W1 (token 2t+1), X holds in each byte the
       // even-dim code of W0 (low nibble) and of W1 (high nibble), Y the
@@ -633,6 +763,30 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
   }
   cp_async_wait<0>();
 
+  if constexpr (MODE == 1) {
+    // ---- the row-maximum pass: the unit's maxima (over the 8 lanes of each
+    // t, then over the warps) stored for the attention pass --------------
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1)
+        mfix[k] = fmaxf(mfix[k], __shfl_xor_sync(0xffffffffu, mfix[k], o));
+    __syncthreads();  // every warp is done with its pipeline buffers
+    float* sMx = reinterpret_cast<float*>(pipe);  // [WARPS][RB]
+    if (g == 0) {
+      sMx[warp * T::RB + 2 * t] = mfix[0];
+      sMx[warp * T::RB + 2 * t + 1] = mfix[1];
+    }
+    __syncthreads();
+    if (tid < T::RB && row0 + tid < R) {
+      const int r = row0 + tid;
+      float m = -INFINITY;
+      for (int w = 0; w < WARPS; ++w) m = fmaxf(m, sMx[w * T::RB + tid]);
+      p.row_max[((int64_t)(u.qo_begin + r / G) * p.num_qo_heads + u.h_kv * G + r % G) *
+                    p.row_max_splits + u.split] = m;
+    }
+    return;
+  }
   // ---- combine the warps ------------------------------------------------
   if constexpr (NT == 1) {  // rows 2t, 2t+1: sum over the 8 lanes of the same t
 #pragma unroll
@@ -655,8 +809,16 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
     if (g == 0) {
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        sM[warp * T::RB + 2 * t + k] = mrow[k];
-        sL[warp * T::RB + 2 * t + k] = lrow[k];
+        if constexpr (MODE == 2) {
+          // the row sum carries the scale of p and the maximum drops it, so
+          // the combine divides o by 2688 * sum p and lse = m + log2(sum p);
+          // a warp that saw no key of the row contributes nothing
+          sM[warp * T::RB + 2 * t + k] = lrow[k] > 0.f ? mfix[k] - kLog2PScale : -INFINITY;
+          sL[warp * T::RB + 2 * t + k] = lrow[k] * kPScale;
+        } else {
+          sM[warp * T::RB + 2 * t + k] = mrow[k];
+          sL[warp * T::RB + 2 * t + k] = lrow[k];
+        }
       }
     }
   } else if (t == 0) {
@@ -690,7 +852,7 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
 #define NVFP4KV_TC_STAGES 4
 #endif
 
-template <int DK, int DV, int NT>
+template <int DK, int DV, int NT, int MODE = 0>
 bool make_tc(AttendConfig* cfg) {
   // 512-wide K rows: 8 warps per CTA (one CTA per SM by shared memory, and
   // twice the warps streaming pages): 30.9 against 42.3 us on the 512/256
@@ -698,14 +860,14 @@ bool make_tc(AttendConfig* cfg) {
   constexpr int WARPS = DK >= 512 ? 8 : NVFP4KV_TC_WARPS;
   constexpr int STAGES = DK >= 512 ? 3 : NVFP4KV_TC_STAGES;
   using T = TcTraits<DK, DV, NT, WARPS, STAGES>;
-  cfg->kind = kKernelTensorCore;
+  cfg->kind = MODE == 0 ? kKernelTensorCore : kKernelFp4QP;
   cfg->dk = DK;
   cfg->dv = DV;
   cfg->rows = T::RB;
   cfg->warps = WARPS;
   cfg->smem_bytes = T::SMEM;
   cfg->func =
-      reinterpret_cast<const void*>(attend_tc_kernel<DK, DV, NT, WARPS, STAGES>);
+      reinterpret_cast<const void*>(attend_tc_kernel<DK, DV, NT, WARPS, STAGES, MODE>);
   return true;
 }
 
@@ -721,6 +883,16 @@ bool attend_config_tc(int dk, int dv, int rows, AttendConfig* cfg) {
   NVFP4KV_TC_CASE(256, 128)
   NVFP4KV_TC_CASE(512, 256)
 #undef NVFP4KV_TC_CASE
+  return false;
+}
+
+// The FP4 query and probabilities kernels (one row block of <= 8 rows): pass
+// 1 writes the units' row maxima, pass 2 attends with them.
+bool attend_config_tc_fp4qp(int dk, int dv, int rows, int pass, AttendConfig* cfg) {
+  if (rows > 8 || (pass != 1 && pass != 2)) return false;
+  if (dk == 64 && dv == 64) return pass == 1 ? make_tc<64, 64, 1, 1>(cfg) : make_tc<64, 64, 1, 2>(cfg);
+  if (dk == 128 && dv == 128)
+    return pass == 1 ? make_tc<128, 128, 1, 1>(cfg) : make_tc<128, 128, 1, 2>(cfg);
   return false;
 }
 

@@ -76,6 +76,11 @@ struct AttendParams {
   const uint16_t* new_v;
   int64_t nk_stride_tok, nk_stride_head, nv_stride_tok, nv_stride_head;
   float k_global_scale, v_global_scale;
+  // FP4 query and probabilities (kernel 4): the row maxima (log2 domain) of
+  // query row i, head h over split s of its request, at
+  //   row_max[((qo_begin + i) * Hq + h) * row_max_splits + s]
+  float* row_max;
+  int32_t row_max_splits;
 };
 
 struct AppendParams {
@@ -116,7 +121,8 @@ struct DequantParams {
 };
 
 // Kernel families and their launch descriptions (defined in the .cu files).
-enum KernelKind { kKernelTensorCore = 1, kKernelCudaCore = 2, kKernelTcgen05 = 3 };
+enum KernelKind { kKernelTensorCore = 1, kKernelCudaCore = 2, kKernelTcgen05 = 3,
+                  kKernelFp4QP = 4 };
 
 struct AttendConfig {
   int kind;       // KernelKind

@@ -355,3 +355,28 @@ def test_plan_rejects_other_page_sizes_and_dtypes():
         plan(batch, out_dtype=torch.float32)
     p = plan(batch, out_dtype=torch.float16)
     assert p.info.out_dtype == 1
+
+
+def test_plan_fp4qp_row_max_region():
+    """kernel=4 (FP4 query and probabilities) plans the mma.sync work list and
+    a row-maximum region of rows x Hq x units-per-request floats after the
+    partial states; it takes one block of at most 8 query rows and head dims
+    64 or 128."""
+    batch = W.make_batch(W.custom_workload(batch=3, qo_len=1, num_qo_heads=8, num_kv_heads=2,
+                                           kv_lens=(40, 3000, 9000)))
+    p = plan(batch, kernel=4)
+    i = p.info
+    assert i.kernel == 4 and i.rows_per_block == 8
+    check_cover(batch, p)
+    assert i.off_row_max >= i.off_partial_o and i.off_row_max % 256 == 0
+    need = i.total_qo_rows * i.num_qo_heads * max(i.max_units_per_request, 1) * 4
+    assert i.workspace_bytes >= i.off_row_max + need
+    assert plan(batch, kernel=1).info.off_row_max == 0
+    ext = W.make_batch(W.custom_workload(batch=2, qo_len=4, num_qo_heads=8, num_kv_heads=2,
+                                         kv_lens=(100, 900), causal=True))
+    with pytest.raises(N.NvFp4KvError):      # 16 rows per kv head
+        plan(ext, kernel=4)
+    wide = W.make_batch(W.custom_workload(batch=1, head_dim_qk=256, head_dim_vo=256,
+                                          kv_lens=(100,)))
+    with pytest.raises(N.NvFp4KvError):
+        plan(wide, kernel=4)
