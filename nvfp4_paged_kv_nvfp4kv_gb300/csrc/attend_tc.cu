@@ -47,7 +47,7 @@
 // block of <= 8 rows, two launches of this kernel:
 //  * MODE 1 quantises each 16-dim block of Q to NVFP4 (global scale 1, the
 //    cache's exact recipe), takes the scores like MODE 0 and stores each
-//    unit's row maxima (no V, no PV);
+//    unit's row maxima (its page copies skip V; no PV);
 //  * MODE 2 reads the maxima of all units of the request, takes p = 2^(x -
 //    m) (m the row's maximum over all its keys), and per row and 16-token
 //    tile quantises 2688 p to NVFP4: E4M3 scale RN(max / 6), e2m1 codes by
@@ -216,10 +216,11 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
       pid = 0;
     }
     uint8_t* st = wpipe + (i % STAGES) * T::STAGE_BYTES;
+    // the row-maximum pass (MODE 1) reads no V
     if (rows)
-      issue_tile_rows<typename T::S>(st, p.cache, pid, u.h_kv, lane);
+      issue_tile_rows<typename T::S, MODE != 1>(st, p.cache, pid, u.h_kv, lane);
     else
-      issue_page<typename T::S>(st, p.cache, pid, u.h_kv, lane);
+      issue_page<typename T::S, MODE != 1>(st, p.cache, pid, u.h_kv, lane);
   };
 
 #pragma unroll

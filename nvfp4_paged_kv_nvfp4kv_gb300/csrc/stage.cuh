@@ -40,8 +40,9 @@ struct PageStage {
   }
 };
 
-// Copy one page (16 tokens of kv head h, page id pid) into a warp's stage.
-template <class S>
+// Copy one page (16 tokens of kv head h, page id pid) into a warp's stage
+// (without WITH_V: its K rows and K scales only).
+template <class S, bool WITH_V = true>
 __device__ __forceinline__ void issue_page(uint8_t* st, const CacheView& c, int32_t pid,
                                            int h, int lane) {
   using namespace dev;
@@ -57,7 +58,7 @@ __device__ __forceinline__ void issue_page(uint8_t* st, const CacheView& c, int3
     cp_async_16(st + r * S::KROW + S::k_pos(r, ch) * 16, kb + r * c.k_ss + ch * 16);
   }
 #pragma unroll
-  for (int ci = lane; ci < 16 * VCHR; ci += 32) {
+  for (int ci = lane; WITH_V && ci < 16 * VCHR; ci += 32) {
     const int r = ci / VCHR, ch = ci % VCHR;
     cp_async_16(st + S::OFF_V + r * S::VROW + ch * 16, vb + r * c.v_ss + ch * 16);
   }
@@ -72,7 +73,7 @@ __device__ __forceinline__ void issue_page(uint8_t* st, const CacheView& c, int3
   constexpr int VSU = S::VSFROW < 16 ? S::VSFROW : 16;
   constexpr int VSN = S::VSFROW / VSU;
 #pragma unroll
-  for (int ci = lane; ci < 16 * VSN; ci += 32) {
+  for (int ci = lane; WITH_V && ci < 16 * VSN; ci += 32) {
     const int r = ci / VSN, u = ci % VSN;
     cp_async_small<VSU>(st + S::OFF_VSF + r * S::VSFROW + u * VSU,
                         vsb + r * c.vsf_ss + u * VSU);
@@ -83,7 +84,7 @@ __device__ __forceinline__ void issue_page(uint8_t* st, const CacheView& c, int3
 // pid_lane: lane r (r < 16) holds the page id of row r (lanes 16-31 repeat
 // lanes 0-15); every lane takes the id of the row it copies by a shuffle,
 // executed by all lanes before the copy's own condition.
-template <class S>
+template <class S, bool WITH_V = true>
 __device__ __forceinline__ void issue_tile_rows(uint8_t* st, const CacheView& c,
                                                 int32_t pid_lane, int h, int lane) {
   using namespace dev;
@@ -99,7 +100,7 @@ __device__ __forceinline__ void issue_tile_rows(uint8_t* st, const CacheView& c,
                   c.k_data + pr * c.k_sp + h * c.k_sh + ch * 16);
   }
 #pragma unroll
-  for (int k = 0; k < (16 * VCHR + 31) / 32; ++k) {
+  for (int k = 0; k < (WITH_V ? (16 * VCHR + 31) / 32 : 0); ++k) {
     const int ci = lane + 32 * k;
     const int r = ci / VCHR, ch = ci % VCHR;
     const int32_t pr = __shfl_sync(0xffffffffu, pid_lane, r & 15);
@@ -121,7 +122,7 @@ __device__ __forceinline__ void issue_tile_rows(uint8_t* st, const CacheView& c,
   constexpr int VSU = S::VSFROW < 16 ? S::VSFROW : 16;
   constexpr int VSN = S::VSFROW / VSU;
 #pragma unroll
-  for (int k = 0; k < (16 * VSN + 31) / 32; ++k) {
+  for (int k = 0; k < (WITH_V ? (16 * VSN + 31) / 32 : 0); ++k) {
     const int ci = lane + 32 * k;
     const int r = ci / VSN, u = ci % VSN;
     const int32_t pr = __shfl_sync(0xffffffffu, pid_lane, r & 15);
