@@ -466,7 +466,7 @@ int orc_attention_unit_fp4qp(const orc_cache* c, const orc_page_table* pt,
                                        (h_kv * G + g) * q_stride_head + d + t]);
         fp4_round16(x, qv + (int64_t)r * dk + d);
       }
-      limit[r] = causal ? (L - nq + i) : (L - 1);
+      limit[r] = causal ? L - nq + i : L - 1;
     }
   /* scores with the quantised query, the row maxima and sums of exp */
   for (j = 0; j < L; ++j) {

@@ -51,6 +51,8 @@ MUTANTS = {
     "fp4qp_mask_ignored_in_p": ("(j < L && j <= limit[r]) ? kPScale", "(j < L) ? kPScale"),
     "fp4qp_p_scaled_by_6_only": ("const double kPScale = 448.0 * 6.0;",
                                  "const double kPScale = 6.0;"),
+    "fp4qp_causal_top_left": ("limit[r] = causal ? L - nq + i : L - 1;",
+                              "limit[r] = causal ? i : L - 1;"),
     "fp4qp_lse_keeps_p_scale": ("-INFINITY : M[r] + log(Z[r]);",
                                 "-INFINITY : M[r] + log(kPScale * Z[r]);"),
     "kv_len_page_size_fixed_at_16": (
