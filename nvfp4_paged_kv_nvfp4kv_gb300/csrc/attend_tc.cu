@@ -534,8 +534,9 @@ __global__ void __launch_bounds__(WARPS * 32, (tc_min_blocks<DK, DV, NT>()))
         mfix[1] = fmaxf(mfix[1], fmaxf(x[1], x[3]));
       } else if constexpr (MODE == 2) {
         // p against the row's maximum over all its keys, scaled by 448 * 6;
-        // per row, the page's 16 values (the 8 lanes of the same t) share an
-        // E4M3 scale RN(max / 6) and each becomes an e2m1 value times it
+        // per row, the tile's 16 values (2 in each of the 8 lanes of the same
+        // t) share an E4M3 scale RN(max / 6) and each becomes an e2m1 value
+        // times it (masked keys have p = 0)
         float pp[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k)
