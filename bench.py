@@ -662,7 +662,10 @@ def run_reference(args, world, rank):
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "cpu_count": cores, "cpu_model": cpu_model(),
                          "sample": "%d (request, kv head) units of requests %s per step, one "
-                                   "per thread" % (n_units, sorted({b for b, _ in units}))},
+                                   "per thread: append of their new tokens + float64 %s" % (
+                                       n_units, sorted({b for b, _ in units}),
+                                       "FP4 query and probabilities attention"
+                                       if args.kernel == 4 else "exact attention")},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
