@@ -77,3 +77,43 @@ def test_fp4qp_fused_append():
     (ro, rl), oc = fp4qp_oracle(batch)
     H.compare_cache_bytes(g.cache, oc)
     record("fused_append", H.compare(out, lse, ro, rl))
+
+
+def test_fp4qp_page_size_one_and_f16_out():
+    """1-token pages in a permuted pool (a 16-key block of P spans 16 pages)
+    with f16 outputs and 256-token chunks."""
+    base = W.make_batch(W.custom_workload(seed=47, batch=3, kv_lens=(37, 300, 1500), qo_len=1,
+                                          num_qo_heads=8, num_kv_heads=1))
+    batch = W.with_page_size_one(base)
+    g = H.GpuCase(batch, kernel=4, out_dtype=torch.float16, force_chunk_tokens=256)
+    assert g.plan.info.kernel == 4 and g.plan.info.split and g.plan.info.page_size == 1
+    out, lse = g.run()
+    assert out.dtype == torch.float16
+    assert N.nvfp4kv_workspace_flags(g.plan) == 0
+    (ro, rl), _ = fp4qp_oracle(batch)
+    record("page_size_one_f16", H.compare(out, lse, ro, rl))
+
+
+def test_fp4qp_live_lengths():
+    """A plan with live last-page lengths: both launches read the current
+    lengths (the row maxima and the attention agree on the keys)."""
+    import test_gpu_live_length as LL
+    full = (22, 40, 105, 250, 1000, 3000)
+    cut = [L - 5 for L in full]
+    batch = LL.batch_of(full, qo_len=1)
+    g = H.GpuCase(batch, append=False)
+    g.append(LL.tokens_below(batch, full))
+    c = batch.cfg
+    np_ = (batch.kv_indptr[1:] - batch.kv_indptr[:-1]).tolist()
+    live = H.dev_i32([L - (n - 1) * 16 for L, n in zip(cut, np_)])
+    plan = N.nvfp4kv_decode_plan(batch.qo_indptr, batch.kv_indptr, batch.last_page_len,
+                                 c.num_qo_heads, c.num_kv_heads, c.head_dim_qk, c.head_dim_vo,
+                                 kernel=4, force_chunk_tokens=128, device_last_page_len=live)
+    assert plan.info.kernel == 4 and plan.info.split == 1
+    out, lse = g.run(plan)
+    assert N.nvfp4kv_workspace_flags(plan) == 0
+    oc, pt = LL.oracle_at(batch, cut)
+    ro, rl = O.attention_fp4qp(oc, pt, batch.qo_indptr, batch.q, c.num_qo_heads, False,
+                               batch.sm_scale)
+    record("live_lengths", H.compare(out, lse, ro, rl))
+

@@ -108,3 +108,24 @@ def test_static_workspace_rejected_call_leaves_the_array_alone():
                                     out=out)
     assert err.value.status == _lib.ERR_INVALID_ARGUMENT
     assert N.nvfp4kv_static_workspace_flags(plan, clear=True) & _lib.FLAG_BAD_PAGE_INDEX
+
+
+def test_fp4qp_static_entry_point():
+    """The allocation-free entry point runs both launches of a kernel-4 plan
+    (the row maxima in its fixed array) and gives the allocating entry
+    point's outputs bit for bit."""
+    batch = W.make_batch(W.custom_workload(seed=31, batch=4, kv_lens=(37, 300, 1000, 2500),
+                                           qo_len=1, num_qo_heads=16, num_kv_heads=4))
+    g = H.GpuCase(batch, kernel=4, force_chunk_tokens=64)
+    ref_out, ref_lse = g.run()
+    plan = host_plan(batch, kernel=4, force_chunk_tokens=64)
+    assert plan.info.kernel == 4 and plan.info.off_row_max > 0
+    rows, c = int(batch.qo_indptr[-1]), batch.cfg
+    out = torch.full((rows, c.num_qo_heads, c.head_dim_vo), float("nan"),
+                     dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((rows, c.num_qo_heads), float("nan"), device="cuda")
+    N.nvfp4kv_decode_run_static(plan, g.q, g.cache, g.kv_indices, batch.sm_scale, out=out,
+                                lse=lse)
+    torch.cuda.synchronize()
+    assert N.nvfp4kv_static_workspace_flags(plan) == 0
+    assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
