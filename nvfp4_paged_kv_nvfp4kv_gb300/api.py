@@ -165,7 +165,10 @@ def nvfp4kv_decode_plan(qo_indptr, kv_indptr, last_page_len, num_qo_heads: int,
     enough (one library call, no allocation).  ``device_last_page_len`` (an
     int32 device tensor [batch]) makes every run read the current last page
     lengths from it (the plan stays valid while page and query counts do).
-    ``out_dtype`` is torch.bfloat16 (default) or torch.float16."""
+    ``out_dtype`` is torch.bfloat16 (default) or torch.float16.  ``kernel``:
+    0 auto, 1 tensor-core mma.sync, 2 CUDA-core, 3 tcgen05 (head dims 128),
+    4 FP4 query and probabilities (at most 8 query rows per kv head, head
+    dims 64 or 128; two launches per run), as in nvfp4kv.h."""
     if out_dtype not in (torch.bfloat16, torch.float16):
         raise ValueError("out_dtype must be torch.bfloat16 or torch.float16")
     L = _lib.load()
